@@ -1,0 +1,162 @@
+"""CPU oracle for tiled scaled-dot-product attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+Python binding) never touches it, and it never touches the product: the two
+share no code.
+
+``attn`` materialises each score row in float64 (attention.fkc.md,
+"attention_naive"); ``attn_tiled`` runs the streaming online-softmax
+recurrence (attention.fkc.md, "attention_flash"; "gfx942 unified attention",
+section 3) in float64 and exists to cross-check the first.  Decode is the same
+definition with one query row and no causal mask ("gfx942 unified attention",
+section 4, last paragraph), so ``decode`` calls ``attn`` with Sq = 1.
+
+Parity pins: every function here is pinned by tests/test_oracle_pins.py
+(closed forms, brute force, library special cases, invariants); none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_DT = {torch.bfloat16: 0, torch.float32: 1, torch.float64: 2}
+
+
+def build(force: bool = False) -> str:
+    """Compile attn_oracle.c into liboracle.so next to it (gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                        "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            L = ctypes.c_long
+            Dd = ctypes.c_double
+            lib.oracle_attn_rows.argtypes = [I, P, P, P, P, P, I, I, I, I, I, I, Dd, I, L, L, Dd,
+                                             P, ctypes.c_int64, P, P, I]
+            lib.oracle_attn_rows.restype = I
+            lib.oracle_attn_tiled.argtypes = [I, P, P, P, P, P, I, I, I, I, I, I, Dd, I, L, L, Dd,
+                                              I, I, P, P, I]
+            lib.oracle_attn_tiled.restype = I
+            lib.oracle_max_threads.restype = I
+            _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return _load().oracle_max_threads()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _prep(q, k, v, alibi_slopes, row_kv_bounds):
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DT:
+        raise TypeError("q, k, v must share one of bf16 / f32 / f64")
+    q, k, v = (t.detach().to("cpu").contiguous() for t in (q, k, v))
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q [B,Hq,Sq,D], k and v [B,Hkv,Sk,D]")
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if Bk != B or Dk != D or Hq % Hkv:
+        raise ValueError("shape mismatch or Hq not a multiple of Hkv")
+    s = None if alibi_slopes is None else alibi_slopes.detach().to("cpu", torch.float32).contiguous()
+    if s is not None and s.numel() != Hq:
+        raise ValueError("alibi slopes must be [Hq]")
+    rb = None if row_kv_bounds is None else row_kv_bounds.detach().to("cpu", torch.int32).contiguous()
+    if rb is not None and tuple(rb.shape) != (B, Sq, 2):
+        raise ValueError("row_kv_bounds must be [B, Sq, 2]")
+    return q, k, v, s, rb, (B, Hq, Hkv, Sq, Sk, D)
+
+
+def _f32(x: float) -> float:
+    """The float32 value the GPU receives, as a Python float."""
+    return float(torch.tensor(x, dtype=torch.float32))
+
+
+def _win(w):
+    return -1 if w is None or w < 0 else int(w)
+
+
+def attn(q, k, v, *, scale=None, causal=False, window_left=None, window_right=None,
+         softcap=None, alibi_slopes=None, row_kv_bounds=None, rows=None, threads=0,
+         return_lse=False):
+    """Materialised float64 attention.
+
+    q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] (bf16, f32 or f64, any device: copied to
+    the host).  ``rows`` (optional 1-D int64 of flat (b*Hq + h)*Sq + qi
+    indices) restricts the work to those rows; the result is then [n, D].
+    Returns float64 out (and lse if asked).
+    """
+    q, k, v, s, rb, (B, Hq, Hkv, Sq, Sk, D) = _prep(q, k, v, alibi_slopes, row_kv_bounds)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    if rows is None:
+        out = torch.empty(B, Hq, Sq, D, dtype=torch.float64)
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float64)
+        rr, n = None, 0
+    else:
+        rr = torch.as_tensor(rows, dtype=torch.int64).contiguous()
+        n = rr.numel()
+        if n and (int(rr.min()) < 0 or int(rr.max()) >= B * Hq * Sq):
+            raise ValueError("row index out of range")
+        out = torch.empty(n, D, dtype=torch.float64)
+        lse = torch.empty(n, dtype=torch.float64)
+    rc = _load().oracle_attn_rows(_DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(rb),
+                                  B, Hq, Hkv, Sq, Sk, D, _f32(scale), int(bool(causal)),
+                                  _win(window_left), _win(window_right),
+                                  0.0 if not softcap else _f32(softcap),
+                                  _ptr(rr), n, _ptr(out), _ptr(lse), int(threads))
+    if rc:
+        raise ValueError("oracle rejected the problem")
+    return (out, lse) if return_lse else out
+
+
+def attn_tiled(q, k, v, *, BR=16, BC=16, scale=None, causal=False, window_left=None,
+               window_right=None, softcap=None, alibi_slopes=None, row_kv_bounds=None,
+               threads=0, return_lse=False):
+    """Streaming (online-softmax) float64 attention over BR x BC tiles."""
+    q, k, v, s, rb, (B, Hq, Hkv, Sq, Sk, D) = _prep(q, k, v, alibi_slopes, row_kv_bounds)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    out = torch.empty(B, Hq, Sq, D, dtype=torch.float64)
+    lse = torch.empty(B, Hq, Sq, dtype=torch.float64)
+    rc = _load().oracle_attn_tiled(_DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(rb),
+                                   B, Hq, Hkv, Sq, Sk, D, _f32(scale), int(bool(causal)),
+                                   _win(window_left), _win(window_right),
+                                   0.0 if not softcap else _f32(softcap),
+                                   int(BR), int(BC), _ptr(out), _ptr(lse), int(threads))
+    if rc:
+        raise ValueError("oracle rejected the problem")
+    return (out, lse) if return_lse else out
+
+
+def decode(q, k, v, *, scale=None, softcap=None, alibi_slopes=None, rows=None, threads=0,
+           return_lse=False):
+    """Decode: one query row per (b, h) attending to every key, no causal mask."""
+    if q.shape[2] != 1:
+        raise ValueError("decode takes Sq == 1")
+    return attn(q, k, v, scale=scale, causal=False, softcap=softcap, alibi_slopes=alibi_slopes,
+                rows=rows, threads=threads, return_lse=return_lse)
