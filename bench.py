@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 attention path (one JSON line on stdout).
+
+A step is one pass of the hot path over one batch of synthetic input:
+  * prefill (the headline): attn_fwd on bf16 causal prefill B=4, Hq=32,
+    Hkv=8, S=2048, D=128 (rows a1-a8 of the path), inputs resident in HBM;
+  * decode (reported beside it): attn_decode on bf16 B=64, Hq=32, Hkv=8,
+    Sk=8192, D=128 (rows a9-a10).
+value = causal-adjusted attention TFLOP/s (4 D flops per admissible
+(query, key) pair) over all ranks.  The decode object reports HBM GB/s of its
+algorithmic bytes (Q + K + V + O).
+
+--impl reference runs the float64 CPU oracle (the only other implementation
+of the method here) on a bounded row sample of the same workload.
+
+Multi-GPU: one process per GPU (torchrun); the workload is replicated per GPU
+(independent problems, no collective on the data path): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (causal-adj) & decode HBM GB/s, % of roofline, 1×GB300"
+PREFILL = "bf16_causal_b4_h32_s2048_d128"
+DECODE = "bf16_decode_b64_h32_sk8192_d128"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gbattn", choices=["gbattn", "reference"])
+    ap.add_argument("--workload", default=PREFILL, choices=[n for n in WORKLOADS if not WORKLOADS[n].decode])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
+    ap.add_argument("--profile", action="store_true", help="kernel launches only (for an ncu launch list)")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- environment
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling of one GPU while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        if not shutil.which("nvidia-smi"):
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.out = open(self.path, "w")
+        self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                      "-lms", "100", "-i", str(self.gpu)], stdout=self.out,
+                                     stderr=subprocess.DEVNULL)
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]), power=float(parts[3]),
+                                     hw=parts[5], hwt=parts[6], swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        busy = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in busy:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"), ("swt", "sw_thermal_slowdown"),
+                              ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in busy), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy), "power_w_max": max(r["power"] for r in rows)}
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def prefill_call(g, w, x, out):
+    return g.attn_fwd(x["q"], x["k"], x["v"], x["alibi_slopes"], softmax_scale=w.scale, causal=w.causal,
+                      window_left=w.window_left, window_right=w.window_right, softcap=w.softcap,
+                      row_kv_bounds=x["row_kv_bounds"], out=out)
+
+
+def time_region(fn, steps, ws, stream):
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    return e0.elapsed_time(e1)
+
+
+def soak(fn, seconds):
+    """Untimed back-to-back steps so that clocks settle before the timed region."""
+    t0 = time.time()
+    i = 0
+    while time.time() - t0 < seconds:
+        fn(i)
+        i += 1
+        if i % 50 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+
+
+def bench_prefill(g, w, args, ws, dev, pk):
+    stream = torch.cuda.current_stream()
+    base = make_inputs(w, dev)
+    in_bytes = sum(t.numel() * t.element_size() for k, t in base.items() if k in ("q", "k", "v"))
+    n_copies = max(1, math.ceil(2 * L2_BYTES / in_bytes))  # rotate so no step reads another's data from L2
+    sets = [base] + [{k: (None if t is None else t.clone()) for k, t in base.items()} for _ in range(n_copies - 1)]
+    outs = [torch.empty_like(base["q"]) for _ in range(n_copies)]
+    fn = lambda i: prefill_call(g, w, sets[i % n_copies], outs[i % n_copies])
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    if g.device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+    if args.profile:
+        for i in range(args.steps):
+            fn(i)
+        torch.cuda.synchronize()
+        return None
+    soak(fn, 1.0)
+    ms = time_region(fn, args.steps, ws, stream)
+    ms = max_over_ranks(ms, ws)
+    flops = w.flops(None if base["row_kv_bounds"] is None else base["row_kv_bounds"].cpu())
+    per_launch_ms = ms / args.steps
+    tflops = flops / (per_launch_ms * 1e-3) / 1e12
+    res = dict(ms_per_step=per_launch_ms, tflops_per_gpu=tflops, flops=flops, dense_flops=w.dense_flops(),
+               rotation=n_copies, in_bytes=in_bytes)
+    res["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                       "frac": round(tflops / pk["bf16"], 4), "traffic": None,
+                       "peak_source": f"bf16_tflops ({pk['source']}, burst: the kernel is timed alone)"}
+    if not args.no_e2e:
+        res["e2e"] = e2e_prefill(g, w, base, args, ws, stream, flops)
+    del sets, outs
+    return res
+
+
+def e2e_prefill(g, w, base, args, ws, stream, flops):
+    host = {k: (None if t is None else t.cpu().pin_memory()) for k, t in base.items()}
+    dev = {k: (None if t is None else torch.empty_like(t)) for k, t in base.items()}
+    out_d = torch.empty_like(base["q"])
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype, pin_memory=True)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v"))
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step(i):
+        for k in ("q", "k", "v"):
+            dev[k].copy_(host[k], non_blocking=True)
+        prefill_call(g, w, dev, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for i in range(max(1, args.warmup)):
+        step(i)
+    ms = max_over_ranks(time_region(step, args.steps, ws, stream), ws)
+    tf = flops / (ms / args.steps * 1e-3) / 1e12 * ws
+    return {"value": round(tf, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / args.steps, 4)}
+
+
+def bench_decode(g, args, ws, dev, pk):
+    w = WORKLOADS[DECODE]
+    stream = torch.cuda.current_stream()
+    x = make_inputs(w, dev)
+    out = torch.empty_like(x["q"])
+    ws_bytes = g.decode_workspace_size(w.B, w.Hq, w.Hkv, w.Sk, w.D, 0)
+    wsp = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    fn = lambda i: g.attn_decode(x["q"], x["k"], x["v"], softmax_scale=w.scale, out=out, workspace=wsp)
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    if args.profile:
+        for i in range(args.steps):
+            fn(i)
+        torch.cuda.synchronize()
+        return None
+    soak(fn, 0.5)
+    ms = max_over_ranks(time_region(fn, args.steps, ws, stream), ws)
+    per = ms / args.steps
+    nbytes = w.bytes_moved()
+    gbs = nbytes / (per * 1e-3) / 1e9
+    splits = ws_bytes // (w.B * w.Hq * (w.D + 1) * 4) if ws_bytes else 1
+    res = {"workload": DECODE, "metric": "decode HBM GB/s (Q+K+V+O bytes)", "value": round(gbs * ws, 1),
+           "unit": "GB/s", "ms_per_step": round(per, 4), "bytes_per_step": nbytes,
+           "launches_per_step": 2 if ws_bytes else 1, "splits": int(splits),
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                        "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                        "peak_source": f"hbm_gbs ({pk['source']})", "frac_of_8tbs_nominal": round(gbs / 8000.0, 4)}}
+    if not args.no_e2e:
+        qh = x["q"].cpu().pin_memory()
+        kh = x["k"].cpu().pin_memory()
+        vh = x["v"].cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def step(i):
+            x["q"].copy_(qh, non_blocking=True)
+            x["k"].copy_(kh, non_blocking=True)
+            x["v"].copy_(vh, non_blocking=True)
+            fn(i)
+            oh.copy_(out, non_blocking=True)
+
+        step(0)
+        ms2 = max_over_ranks(time_region(step, max(3, args.steps // 4), ws, stream), ws)
+        per2 = ms2 / max(3, args.steps // 4)
+        res["e2e"] = {"value": round(nbytes / (per2 * 1e-3) / 1e9 * ws, 1), "unit": "GB/s",
+                      "h2d_bytes_per_step": qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2,
+                      "d2h_bytes_per_step": oh.numel() * 2, "ms_per_step": round(per2, 4)}
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def admissible_pairs(w, rows, rb):
+    """Admissible (query, key) pairs of the given flat (b*Hq + h)*Sq + qi rows."""
+    n = 0
+    for r in rows.tolist():
+        qi = r % w.Sq
+        b = r // (w.Sq * w.Hq)
+        a, e = 0, w.Sk - 1
+        if w.causal:
+            e = min(e, qi)
+        if w.window_left is not None:
+            a = max(a, qi - w.window_left)
+        if w.window_right is not None:
+            e = min(e, qi + w.window_right)
+        if rb is not None:
+            a, e = max(a, int(rb[b, qi, 0])), min(e, int(rb[b, qi, 1]))
+        n += max(0, e - a + 1)
+    return n
+
+
+def oracle_kwargs(w, x_cpu):
+    return dict(scale=w.scale, causal=w.causal, window_left=w.window_left, window_right=w.window_right,
+                softcap=w.softcap, alibi_slopes=x_cpu["alibi_slopes"], row_kv_bounds=x_cpu["row_kv_bounds"])
+
+
+def oracle_rows(w, x_cpu, seconds, seed=11):
+    """A seeded row sample of the workload that takes the oracle about
+    `seconds`; returns (rows, seconds taken)."""
+    import oracle
+    import synth
+    total_rows = w.B * w.Hq * w.Sq
+    n = 64
+    while True:
+        rows = torch.unique(synth.randint(n, total_rows, seed, 12))
+        t0 = time.time()
+        oracle.attn(x_cpu["q"], x_cpu["k"], x_cpu["v"], rows=rows, **oracle_kwargs(w, x_cpu))
+        dt = time.time() - t0
+        if dt >= seconds or n >= total_rows:
+            return rows, dt
+        n = min(total_rows, int(n * max(1.2, min(16.0, 1.05 * seconds / max(dt, 1e-3))))))
+
+
+def oracle_sample(w, x_cpu, seconds):
+    """CPU baseline: oracle TFLOP/s on a bounded row sample."""
+    import oracle
+    rows, dt = oracle_rows(w, x_cpu, seconds)
+    flops = 4.0 * w.D * admissible_pairs(w, rows, x_cpu["row_kv_bounds"])
+    total = w.B * w.Hq * w.Sq
+    return flops / dt / 1e12, f"{rows.numel()} seeded random query rows of {total} ({dt:.1f} s)", \
+        oracle.max_threads()
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return main_reference(args, ws, rank, w)
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    import tiled_scaled_dot_gb300 as g
+    g.lib()
+    pk = peaks()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else dev.index
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    try:
+        pre = bench_prefill(g, w, args, ws, dev, pk)
+        dec = None if (args.no_decode or args.profile) else bench_decode(g, args, ws, dev, pk)
+        if args.profile:
+            dec = bench_decode(g, args, ws, dev, pk) if not args.no_decode else None
+    finally:
+        clocks = sampler.stop()
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "workload": w.name}))
+        return
+    if g.device_status() != 0:
+        raise RuntimeError("device status word set during the benchmark")
+    total_tf = pre["tflops_per_gpu"] * ws
+    line = {
+        "metric": METRIC, "value": round(total_tf, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(pre["ms_per_step"], 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded SplitMix64 + Box-Muller N(0,1), cast to the storage dtype)",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+                   "causal": w.causal, "flops_per_step": pre["flops"], "dense_flops_per_step": pre["dense_flops"],
+                   "l2": f"inputs rotated over {pre['rotation']} copies ({pre['in_bytes'] / 2**20:.0f} MiB each) "
+                         f"so no step reads data left in L2 by the previous one",
+                   "parallelism": f"replicas x{ws} (no collective)"},
+        "roofline": pre["roofline"],
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if "e2e" in pre:
+        line["e2e"] = pre["e2e"]
+    if dec is not None:
+        line["decode"] = dec
+        line["gpu_launches"] += args.steps * dec["launches_per_step"]
+    if rank == 0 and not args.no_cpu_baseline:
+        x_cpu = make_inputs(w, "cpu")
+        tf, sample, threads = oracle_sample(w, x_cpu, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main_reference(args, ws, rank, w):
+    """The float64 oracle on the host cores, each step a bounded row sample."""
+    if rank != 0:
+        return
+    import oracle
+    x = make_inputs(w, "cpu")
+    # one step is sized to about 3 s so that warm-up + steps end within a few minutes
+    per_step = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows, _ = oracle_rows(w, x, per_step)
+    kw = oracle_kwargs(w, x)
+    for _ in range(args.warmup):
+        oracle.attn(x["q"], x["k"], x["v"], rows=rows, **kw)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.attn(x["q"], x["k"], x["v"], rows=rows, **kw)
+    dt = time.time() - t0
+    flops_step = 4.0 * w.D * admissible_pairs(w, rows, x["row_kv_bounds"])
+    value = flops_step * args.steps / dt / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same seeded inputs as the GPU arm)",
+            "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"{rows.numel()} seeded random query rows of {w.B * w.Hq * w.Sq} per step"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

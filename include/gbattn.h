@@ -1,0 +1,178 @@
+/*
+ * gbattn.h -- C ABI of the GB300 (sm_103a) tiled scaled-dot-product attention
+ * library (libgbattn.so).
+ *
+ * Operation (attention.fkc.md, "attention_naive" and "attention_flash";
+ * "gfx942 unified attention, from the math up", sections 1-4): for every batch
+ * b, query head h and query row i, with kv head g = h / (Hq / Hkv) (the GQA
+ * broadcast stated in the header of attention.fkc.md),
+ *
+ *     s_j = softmax_scale * (Q[b,h,i,:] . K[b,g,j,:])
+ *     s_j = softcap * tanh(s_j / softcap)        when softcap > 0
+ *     s_j = s_j + alibi_slopes[h] * (j - i)      when alibi_slopes != NULL
+ *     s_j = -inf                                 when key j is not admissible
+ *     O[b,h,i,:] = sum_j softmax(s)_j V[b,g,j,:] and lse = log sum_j exp(s_j)
+ *
+ * Admissible (attention.fkc.md, header: position_admissible): not (causal and
+ * j > i), not (window_left >= 0 and j + window_left < i), not (window_right
+ * >= 0 and j > i + window_right), and, in attn_fwd_ex only, lo <= j <= hi for
+ * the row's entry of row_kv_bounds.  A row with no admissible key is the
+ * all-zero row, with lse = -inf (attention.fkc.md, attention_naive).  Causal
+ * alignment is top-left (key j is in the future of query i when j > i), as in
+ * position_admissible.
+ *
+ * The result is computed by the tiled online-softmax recurrence ("gfx942
+ * unified attention", section 3): running max m, denominator l, rescale
+ * alpha = exp(m_old - m_new), final O = o / l.
+ *
+ * Layout (attention.fkc.md, header): every tensor is contiguous, row-major,
+ * zero offset, batch first then heads: q [B, Hq, Sq, D], k and v
+ * [B, Hkv, Sk, D], out [B, Hq, Sq, D], lse [B, Hq, Sq].
+ *
+ * Ownership: the caller owns every buffer.  All pointers are device pointers
+ * of the current CUDA device, 16-byte aligned.  The library allocates no device
+ * memory in any call; it keeps a small host cache of TMA descriptors.  Calls
+ * enqueue work on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ * and return without synchronising.  `out` must not overlap any input.
+ *
+ * Errors: every call returns a status code and never aborts the process.
+ * Argument errors are detected on the host before anything is launched.
+ * GBATTN_ERR_CUDA carries a launch failure (the CUDA error is left in
+ * cudaGetLastError).  A kernel that meets a bounded-wait timeout records it in
+ * a device status word which gbattn_device_status() reads.
+ */
+#ifndef GBATTN_H_
+#define GBATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and out. */
+typedef enum {
+    GBATTN_BF16 = 0, /* bfloat16 storage, fp32 accumulation, bf16 output (RNE)   */
+    GBATTN_F32 = 1   /* float32 storage and arithmetic (SIMT FFMA, no TF32)       */
+} gbattn_dtype;
+
+enum {
+    GBATTN_OK = 0,
+    GBATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, Hq % Hkv != 0, ...        */
+    GBATTN_ERR_UNSUPPORTED = 2, /* valid problem outside what the kernels implement  */
+    GBATTN_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed              */
+    GBATTN_ERR_DEVICE = 4       /* the device status word is set (bounded wait ran out) */
+};
+
+/*
+ * attn_fwd -- multi-head SDPA forward (prefill).
+ * attention.fkc.md, attention_naive / attention_flash (operation and
+ * AttentionParams: softmax_scale, causal, window_size_left/right, softcap,
+ * optional ALiBi slopes [Hq]).
+ *
+ *  q, k, v        device, layout above, element type `dtype`.
+ *  alibi_slopes   device fp32 [Hq] or NULL (no ALiBi).
+ *  out            device [B, Hq, Sq, D], element type `dtype`, written fully.
+ *  B, Hq, Hkv, Sq, Sk, D   sizes, all > 0; Hq % Hkv == 0.
+ *                 D must be 64 or 128 (else GBATTN_ERR_UNSUPPORTED).
+ *  softmax_scale  finite and > 0 (usually 1/sqrt(D)).
+ *  causal         0 or 1.
+ *  window_left, window_right   -1 = unbounded (None), else >= 0.
+ *  softcap        0 = none, else finite and > 0.
+ *  dtype          GBATTN_BF16 or GBATTN_F32.
+ *  stream         cudaStream_t.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, int B, int Hq,
+             int Hkv, int Sq, int Sk, int D, float softmax_scale, int causal, int window_left, int window_right,
+             float softcap, int dtype, void* stream);
+
+/*
+ * attn_fwd_ex -- attn_fwd with two optional extras:
+ *  lse_out        device fp32 [B, Hq, Sq] or NULL: natural-log sum of exp of
+ *                 the admissible scores; -inf for a row with none.  The
+ *                 online recurrence's m + ln(l) ("gfx942 unified attention",
+ *                 section 3).
+ *  row_kv_bounds  device int32 [B, Sq, 2] or NULL: inclusive key range
+ *                 [lo, hi] admitted for query row (b, i) in addition to the
+ *                 mask above; lo > hi admits no key, so the row is zero.
+ *                 (Reading of the pages' "window that masks all keys" for
+ *                 single rows; the same bounds apply to every head.)
+ */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* alibi_slopes;
+    const int32_t* row_kv_bounds;
+    void* out;
+    float* lse_out;
+    int B, Hq, Hkv, Sq, Sk, D;
+    float softmax_scale;
+    int causal;
+    int window_left, window_right;
+    float softcap;
+    int dtype;
+    void* stream;
+} gbattn_fwd_params;
+
+int attn_fwd_ex(const gbattn_fwd_params* p);
+
+/*
+ * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
+ * for this problem and split count (num_splits = 0 picks the split count
+ * attn_decode picks, for the current device).  Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Sk, int D, int num_splits);
+
+/*
+ * attn_decode -- decode step: one query row per (b, h) against all Sk keys.
+ * "gfx942 unified attention", section 4 (decode runs non-causal: the single
+ * query sees every key) and section 8 (split-KV: the keys are split across
+ * thread blocks and the partial softmax-weighted outputs combined).  The
+ * combine is the online recurrence of section 3 applied across splits, in a
+ * fixed split order, so reruns are bitwise identical.
+ *
+ *  q              device [B, Hq, 1, D]; k, v device [B, Hkv, Sk, D].
+ *  alibi_slopes   device fp32 [Hq] or NULL; the query position is i = 0.
+ *  out            device [B, Hq, 1, D]; lse_out device fp32 [B, Hq] or NULL.
+ *  softcap        0 = none, else > 0.
+ *  num_splits     0 = automatic; else the number of key chunks (each chunk is a
+ *                 multiple of 64 keys; chunks past the end are empty).
+ *  workspace      device scratch of at least
+ *                 attn_decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits)
+ *                 bytes, 16-byte aligned (may be NULL when that size is 0).
+ *                 Its contents need no initialisation and are not preserved.
+ *  dtype          GBATTN_BF16 (GBATTN_F32 returns GBATTN_ERR_UNSUPPORTED).
+ *  D              64 or 128.
+ */
+int attn_decode(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, float* lse_out,
+                int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap, int num_splits,
+                void* workspace, size_t workspace_bytes, int dtype, void* stream);
+
+/* Human-readable text of a status code (static storage). */
+const char* gbattn_status_string(int status);
+
+/*
+ * gbattn_device_status -- synchronise `stream`, then return the device status
+ * word of the current device (0 = no kernel met a timeout or bounds fault;
+ * otherwise a bitmask of the wait sites that gave up) and clear it when
+ * `clear` is non-zero.  Returns (unsigned)-1 if the synchronisation failed.
+ */
+unsigned int gbattn_device_status(void* stream, int clear);
+
+/*
+ * gbattn_set_wait_timeout_ns -- limit of every bounded wait inside the
+ * kernels (default 2e9 ns; the environment variable GBATTN_WAIT_TIMEOUT_MS
+ * overrides the default at load time).  Returns the previous value.
+ */
+uint64_t gbattn_set_wait_timeout_ns(uint64_t ns);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int gbattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H_ */

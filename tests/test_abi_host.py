@@ -1,0 +1,102 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+symbol the headers declare, and rejects bad arguments before launching
+anything (these calls never reach a kernel, so they need no GPU)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from tiled_scaled_dot_gb300 import build
+    build.build()
+    import tiled_scaled_dot_gb300 as g
+    return g.lib()
+
+
+def _declared_functions():
+    names = []
+    for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(([^;{}]*)\)\s*;", text):
+            names.append(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = _declared_functions()
+    for expected in ("attn_fwd", "attn_fwd_ex", "attn_decode", "attn_decode_workspace_size",
+                     "gbattn_status_string", "gbattn_device_status", "gbattn_set_wait_timeout_ns",
+                     "gbattn_version", "gbattn_diag_umma"):
+        assert expected in names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for st in range(0, 5):
+        assert L.gbattn_status_string(st)
+    assert L.gbattn_status_string(99) == b"unknown status"
+    assert L.gbattn_version() >= 100
+
+
+FAKE = 1 << 20  # a non-null, 16-byte aligned pseudo pointer; never dereferenced on these paths
+
+
+def _fwd(L, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, alibi=None, out=FAKE * 4, B=1, Hq=2, Hkv=1, Sq=64, Sk=64, D=64,
+             scale=0.125, causal=0, wl=-1, wr=-1, softcap=0.0, dtype=0, stream=None)
+    a.update(kw)
+    return L.attn_fwd(a["q"], a["k"], a["v"], a["alibi"], a["out"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"],
+                      a["D"], a["scale"], a["causal"], a["wl"], a["wr"], a["softcap"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=0), 1), (dict(Hq=3, Hkv=2), 1), (dict(Sq=0), 1), (dict(Sk=-1), 1),
+    (dict(q=None), 1), (dict(out=None), 1), (dict(scale=0.0), 1), (dict(scale=float("nan")), 1),
+    (dict(softcap=-1.0), 1), (dict(wl=-2), 1), (dict(causal=2), 1), (dict(dtype=7), 1),
+    (dict(q=FAKE + 2), 1), (dict(out=FAKE), 1),  # misaligned; out aliasing q
+    (dict(D=96), 2), (dict(D=256), 2),
+])
+def test_forward_rejects_bad_arguments(L, kw, status):
+    assert _fwd(L, **kw) == status
+
+
+def test_decode_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    base = [P(FAKE), P(FAKE * 2), P(FAKE * 3), None, P(FAKE * 4), None, 2, 4, 2, 128, 128, 0.1, 0.0, 0,
+            None, 0, 0, None]
+    def call(i, val):
+        a = list(base)
+        a[i] = val
+        return L.attn_decode(*a)
+    assert call(6, 0) == 1          # B = 0
+    assert call(8, 3) == 1          # Hq % Hkv
+    assert call(10, 96) == 2        # D
+    assert call(16, 1) == 2         # fp32 decode not built
+    assert call(13, -1) == 1        # negative split count
+    assert L.attn_decode_workspace_size(0, 4, 2, 128, 128, 0) == 0
+    assert L.attn_decode_workspace_size(2, 4, 2, 8192, 128, 1) == 0
+    n = L.attn_decode_workspace_size(2, 4, 2, 8192, 128, 4)
+    assert n >= 2 * 4 * 4 * (128 + 1) * 4
+    # a split count above the tile count is clamped to one split per 64 keys
+    assert L.attn_decode_workspace_size(1, 1, 1, 128, 64, 1000) == L.attn_decode_workspace_size(1, 1, 1, 128, 64, 2)
+
+
+def test_fwd_ex_null_params(L):
+    assert L.attn_fwd_ex(None) == 1
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import tiled_scaled_dot_gb300 as g
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        g.attn_fwd(q, q[:, :1], q[:, :1])

@@ -1,0 +1,331 @@
+// api.cu -- the C ABI of libgbattn: argument validation, TMA descriptor
+// encoding (with a small cache), kernel dispatch, device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gbattn.h"
+#include "kernels.h"
+
+namespace gbattn {
+
+// Status word written by kernels whose bounded waits give up.
+__device__ unsigned int g_status_word;
+
+namespace {
+
+std::mutex g_mu;
+uint64_t g_timeout_ns = [] {
+    const char* e = std::getenv("GBATTN_WAIT_TIMEOUT_MS");
+    if (e && *e) {
+        long long ms = std::atoll(e);
+        if (ms > 0) return static_cast<uint64_t>(ms) * static_cast<uint64_t>(1000000);
+    }
+    return static_cast<uint64_t>(2000000000ull);
+}();
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// Per-device facts (current device): status word address and SM count.
+bool device_facts(unsigned int** status, int* num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return false;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+        g_num_sms[dev] = sms;
+    }
+    *status = g_status_ptr[dev];
+    *num_sms = g_num_sms[dev];
+    return true;
+}
+
+// Small cache of encoded tensor maps keyed by (device, pointer, extents, box).
+struct MapKey {
+    int dev;
+    const void* base;
+    uint64_t cols, rows, planes;
+    uint32_t box_rows;
+    bool operator==(const MapKey& o) const {
+        return dev == o.dev && base == o.base && cols == o.cols && rows == o.rows && planes == o.planes &&
+               box_rows == o.box_rows;
+    }
+};
+constexpr int kCache = 32;
+MapKey g_keys[kCache];
+CUtensorMap g_maps[kCache];
+int g_used = 0, g_next = 0;
+
+bool cached_map(CUtensorMap* out, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
+                uint32_t box_rows) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    MapKey key{dev, base, cols, rows, planes, box_rows};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        for (int i = 0; i < g_used; ++i)
+            if (g_keys[i] == key) {
+                *out = g_maps[i];
+                return true;
+            }
+    }
+    CUtensorMap m;
+    if (!encode_map_bf16_3d(&m, base, cols, rows, planes, box_rows)) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    int slot = g_used < kCache ? g_used++ : (g_next++ % kCache);
+    g_keys[slot] = key;
+    g_maps[slot] = m;
+    *out = m;
+    return true;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b) return false;
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int check_common(int B, int Hq, int Hkv, int S, int Sk, int D, float scale, float softcap, int dtype) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || Sk <= 0 || D <= 0) return GBATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(scale) && scale > 0.f)) return GBATTN_ERR_INVALID_ARG;
+    if (!(std::isfinite(softcap) && softcap >= 0.f)) return GBATTN_ERR_INVALID_ARG;
+    if (dtype != GBATTN_BF16 && dtype != GBATTN_F32) return GBATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GBATTN_ERR_UNSUPPORTED;
+    // 32-bit index limits of the kernels' grids and rows.
+    if ((long long)B * Hq * S > 0x7fffffffLL || (long long)B * Hkv * Sk > 0x7fffffffLL) return GBATTN_ERR_UNSUPPORTED;
+    return GBATTN_OK;
+}
+
+}  // namespace
+
+bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
+                        uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cols, rows, planes};
+    cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" {
+
+int attn_fwd_ex(const gbattn_fwd_params* a) {
+    if (!a) return GBATTN_ERR_INVALID_ARG;
+    int rc = check_common(a->B, a->Hq, a->Hkv, a->Sq, a->Sk, a->D, a->softmax_scale, a->softcap, a->dtype);
+    if (rc) return rc;
+    if (!a->q || !a->k || !a->v || !a->out) return GBATTN_ERR_INVALID_ARG;
+    if (a->causal != 0 && a->causal != 1) return GBATTN_ERR_INVALID_ARG;
+    if (a->window_left < -1 || a->window_right < -1) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->out)) return GBATTN_ERR_INVALID_ARG;
+    if (a->row_kv_bounds && (reinterpret_cast<uintptr_t>(a->row_kv_bounds) & 7u)) return GBATTN_ERR_INVALID_ARG;
+    if (a->lse_out && (reinterpret_cast<uintptr_t>(a->lse_out) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    const size_t esz = a->dtype == GBATTN_BF16 ? 2 : 4;
+    const size_t nq = (size_t)a->B * a->Hq * a->Sq * a->D * esz;
+    const size_t nkv = (size_t)a->B * a->Hkv * a->Sk * a->D * esz;
+    if (overlaps(a->out, nq, a->q, nq) || overlaps(a->out, nq, a->k, nkv) || overlaps(a->out, nq, a->v, nkv))
+        return GBATTN_ERR_INVALID_ARG;
+
+    FwdProblem f{};
+    f.q = a->q;
+    f.k = a->k;
+    f.v = a->v;
+    f.slopes = a->alibi_slopes;
+    f.row_bounds = a->row_kv_bounds;
+    f.out = a->out;
+    f.lse = a->lse_out;
+    f.B = a->B;
+    f.Hq = a->Hq;
+    f.Hkv = a->Hkv;
+    f.Sq = a->Sq;
+    f.Sk = a->Sk;
+    f.D = a->D;
+    f.scale = a->softmax_scale;
+    f.causal = a->causal;
+    f.wl = a->window_left;
+    f.wr = a->window_right;
+    f.softcap = a->softcap;
+    f.timeout_ns = g_timeout_ns;
+    if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(a->stream);
+    cudaError_t e;
+    if (a->dtype == GBATTN_F32) {
+        e = launch_prefill_f32(f, st);
+    } else {
+        CUtensorMap tq, tk, tv;
+        if (!cached_map(&tq, a->q, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128) ||
+            !cached_map(&tk, a->k, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128) ||
+            !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128))
+            return GBATTN_ERR_CUDA;
+        e = launch_prefill_bf16(f, tq, tk, tv, st);
+    }
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int attn_fwd(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, int B, int Hq,
+             int Hkv, int Sq, int Sk, int D, float softmax_scale, int causal, int window_left, int window_right,
+             float softcap, int dtype, void* stream) {
+    gbattn_fwd_params a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.alibi_slopes = alibi_slopes;
+    a.out = out;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.Sq = Sq;
+    a.Sk = Sk;
+    a.D = D;
+    a.softmax_scale = softmax_scale;
+    a.causal = causal;
+    a.window_left = window_left;
+    a.window_right = window_right;
+    a.softcap = softcap;
+    a.dtype = dtype;
+    a.stream = stream;
+    return attn_fwd_ex(&a);
+}
+
+static int decode_plan(int B, int Hq, int Hkv, int Sk, int D, int num_splits, int* splits, int* chunk) {
+    if (check_common(B, Hq, Hkv, 1, Sk, D, 1.f, 0.f, GBATTN_BF16)) return -1;
+    if (num_splits < 0) return -1;
+    unsigned int* st = nullptr;
+    int sms = 0;
+    if (!device_facts(&st, &sms)) sms = 148;
+    decode_split_plan(B, Hkv, Sk, sms, num_splits, splits, chunk);
+    return 0;
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Sk, int D, int num_splits) {
+    int splits = 0, chunk = 0;
+    if (decode_plan(B, Hq, Hkv, Sk, D, num_splits, &splits, &chunk)) return 0;
+    if (splits <= 1) return 0;
+    const size_t rows = (size_t)B * Hq * splits;
+    const size_t o_bytes = rows * D * sizeof(float);
+    return o_bytes + ((rows * sizeof(float) + 15) & ~size_t(15));
+}
+
+int attn_decode(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, float* lse_out,
+                int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap, int num_splits,
+                void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+    int rc = check_common(B, Hq, Hkv, 1, Sk, D, softmax_scale, softcap, dtype);
+    if (rc) return rc;
+    if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !out || num_splits < 0) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GBATTN_ERR_INVALID_ARG;
+    if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    const size_t nq = (size_t)B * Hq * D * 2, nkv = (size_t)B * Hkv * Sk * D * 2;
+    if (overlaps(out, nq, q, nq) || overlaps(out, nq, k, nkv) || overlaps(out, nq, v, nkv))
+        return GBATTN_ERR_INVALID_ARG;
+
+    DecodeProblem f{};
+    if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
+    decode_split_plan(B, Hkv, Sk, f.num_sms, num_splits, &f.num_splits, &f.chunk);
+    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GBATTN_ERR_INVALID_ARG;
+        if (overlaps(workspace, need, out, nq) || overlaps(workspace, need, q, nq) ||
+            overlaps(workspace, need, k, nkv) || overlaps(workspace, need, v, nkv))
+            return GBATTN_ERR_INVALID_ARG;
+        f.ws_o = static_cast<float*>(workspace);
+        f.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + (size_t)B * Hq * f.num_splits * D * 4);
+    }
+    f.q = q;
+    f.k = k;
+    f.v = v;
+    f.slopes = alibi_slopes;
+    f.out = out;
+    f.lse = lse_out;
+    f.B = B;
+    f.Hq = Hq;
+    f.Hkv = Hkv;
+    f.Sk = Sk;
+    f.D = D;
+    f.scale = softmax_scale;
+    f.softcap = softcap;
+    f.timeout_ns = g_timeout_ns;
+    CUtensorMap tk, tv;
+    if (!cached_map(&tk, k, D, Sk, (uint64_t)B * Hkv, 64) || !cached_map(&tv, v, D, Sk, (uint64_t)B * Hkv, 64))
+        return GBATTN_ERR_CUDA;
+    cudaError_t e = launch_decode_bf16(f, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+const char* gbattn_status_string(int status) {
+    switch (status) {
+        case GBATTN_OK: return "ok";
+        case GBATTN_ERR_INVALID_ARG: return "invalid argument";
+        case GBATTN_ERR_UNSUPPORTED: return "unsupported problem";
+        case GBATTN_ERR_CUDA: return "CUDA error";
+        case GBATTN_ERR_DEVICE: return "device status word set (a bounded wait ran out)";
+        default: return "unknown status";
+    }
+}
+
+unsigned int gbattn_device_status(void* stream, int clear) {
+    unsigned int* st = nullptr;
+    int sms = 0;
+    if (!device_facts(&st, &sms)) return ~0u;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned int v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ~0u;
+    if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof v) != cudaSuccess) return ~0u;
+    if (clear) {
+        unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &z, sizeof z) != cudaSuccess) return ~0u;
+    }
+    return v;
+}
+
+uint64_t gbattn_set_wait_timeout_ns(uint64_t ns) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    uint64_t old = g_timeout_ns;
+    g_timeout_ns = ns;
+    return old;
+}
+
+int gbattn_version(void) { return 100; }
+
+}  // extern "C"

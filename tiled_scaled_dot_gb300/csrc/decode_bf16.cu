@@ -1,0 +1,463 @@
+// decode_bf16.cu -- split-KV decode (one query row per head) and the
+// log-sum-exp combine of the partial results.
+//
+// "gfx942 unified attention, from the math up", section 8: with one query
+// row, parallelism comes from splitting the keys across thread blocks and
+// combining the partial softmax-weighted outputs.  The combine is the online
+// recurrence of section 3 applied across splits: LSE = log sum_s e^{lse_s},
+// O = sum_s e^{lse_s - LSE} O_s, evaluated in a fixed split order.
+//
+// The path is bound by HBM reads of K and V, so it runs on the SIMT pipes:
+//   * one CTA per (batch, kv head, head chunk, split); all query heads of a
+//     GQA group (up to GC of them) are served from one read of each key;
+//   * a producer warp streams 64-key K and V tiles with TMA into a 3-stage
+//     shared-memory ring (128-byte swizzle, so the consumers' row reads are
+//     free of bank conflicts);
+//   * four consumer warps take 16 keys of each tile each and keep their own
+//     running (m, l, o) per head, merged once at the end of the split.
+// Scores: lane (key kq, quarter dq) dots D/4 dimensions and the quarters are
+// summed with two shuffles.  P V: lane owns D/32 output dimensions; the
+// probabilities reach it through a small per-warp shared buffer.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int TILE = 64;     // keys per tile
+constexpr int NSTG = 3;      // ring stages
+constexpr int CONSUMERS = 4; // consumer warps
+constexpr int DEC_THREADS = (CONSUMERS + 1) * 32;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+struct DecParams {
+    const __nv_bfloat16* q;
+    __nv_bfloat16* out;
+    float* lse;
+    const float* slopes;
+    float* ws_o;
+    float* ws_lse;
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    int B, Hq, Hkv, Sk, G;
+    int n_chunks;       // head chunks per kv head
+    int num_splits;
+    int chunk_tiles;    // tiles per split
+    int n_tiles;        // tiles over Sk
+    float qscale;       // multiplies q: scale * log2(e) (no softcap) or scale (softcap)
+    float softcap;
+};
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <int D>
+struct DCfg {
+    static constexpr int SLABS = D / 64;
+    static constexpr int SLAB = TILE * 128;           // bytes of one 64-wide slab of a tile
+    static constexpr int TILE_BYTES = TILE * D * 2;   // K or V tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int SMEM = NSTG * STAGE_BYTES + 1024;
+};
+
+// Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled slab.
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+template <int D, int GC, bool SOFTCAP, bool ALIBI>
+__global__ void __launch_bounds__(DEC_THREADS, 2)
+    decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                       const DecParams p) {
+    using C = DCfg<D>;
+    constexpr int DQ = D / 4;    // dims per lane in Q K^T
+    constexpr int DV = D / 32;   // dims per lane in P V
+    extern __shared__ __align__(1024) uint8_t dyn_smem[];
+    __shared__ uint64_t full_bar[NSTG], empty_bar[NSTG];
+    __shared__ int abort_flag;
+    __shared__ __align__(16) float p_s[CONSUMERS][16][GC < 4 ? 4 : GC];
+    __shared__ float red_m[CONSUMERS][GC], red_l[CONSUMERS][GC];
+    __shared__ __align__(16) float red_o[CONSUMERS][GC][D];
+
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // blockIdx.x -> (b, hkv, chunk, split)
+    int rem = blockIdx.x;
+    const int split = rem % p.num_splits;
+    rem /= p.num_splits;
+    const int hc = rem % p.n_chunks;
+    rem /= p.n_chunks;
+    const int hkv = rem % p.Hkv;
+    const int b = rem / p.Hkv;
+    const int t_begin = split * p.chunk_tiles;
+    const int t_end = min(p.n_tiles, t_begin + p.chunk_tiles);
+    const int h0 = hkv * p.G + hc * GC;                     // first query head of this chunk
+    const int n_heads = min(GC, p.G - hc * GC);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NSTG; ++i) {
+            mbar_init(&full_bar[i], 1);
+            mbar_init(&empty_bar[i], CONSUMERS);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    WaitCtl wc{&abort_flag, p.status, p.timeout_ns};
+
+    if (warp == CONSUMERS) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            uint32_t cnt = 0;
+            bool ok = true;
+            const int plane = b * p.Hkv + hkv;
+            for (int t = t_begin; t < t_end; ++t, ++cnt) {
+                const int st = cnt % NSTG;
+                ok = mbar_wait(&empty_bar[st], ((cnt / NSTG) & 1) ^ 1, wc, ST_DECODE_PRODUCER);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
+                uint8_t* ks = ring + st * C::STAGE_BYTES;
+                uint8_t* vs = ks + C::TILE_BYTES;
+#pragma unroll
+                for (int sl = 0; sl < C::SLABS; ++sl) {
+                    tma_load_3d(ks + sl * C::SLAB, &tmK, &full_bar[st], sl * 64, t * TILE, plane);
+                    tma_load_3d(vs + sl * C::SLAB, &tmV, &full_bar[st], sl * 64, t * TILE, plane);
+                }
+            }
+            if (!ok) {
+                const uint32_t n = cnt < (uint32_t)NSTG ? cnt : (uint32_t)NSTG;
+                for (uint32_t i = cnt - n; i < cnt; ++i) mbar_drain(&full_bar[i % NSTG], (i / NSTG) & 1, 100000000ull);
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------------- consumers
+    const int kq = lane >> 2, dq = lane & 3;
+    float qv[GC][DQ];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        const bool hv = h < n_heads;
+        const __nv_bfloat16* qp = p.q + (size_t)(b * p.Hq + h0 + (hv ? h : 0)) * D + dq * DQ;
+#pragma unroll
+        for (int d = 0; d < DQ; d += 8) {
+            uint4 w = hv ? *reinterpret_cast<const uint4*>(qp + d) : make_uint4(0, 0, 0, 0);
+            qv[h][d + 0] = bf16lo(w.x) * p.qscale;
+            qv[h][d + 1] = bf16hi(w.x) * p.qscale;
+            qv[h][d + 2] = bf16lo(w.y) * p.qscale;
+            qv[h][d + 3] = bf16hi(w.y) * p.qscale;
+            qv[h][d + 4] = bf16lo(w.z) * p.qscale;
+            qv[h][d + 5] = bf16hi(w.z) * p.qscale;
+            qv[h][d + 6] = bf16lo(w.w) * p.qscale;
+            qv[h][d + 7] = bf16hi(w.w) * p.qscale;
+        }
+    }
+    float slope_l2[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) slope_l2[h] = (ALIBI && h < n_heads) ? p.slopes[h0 + h] * LOG2E : 0.f;
+
+    float m[GC], l[GC], o[GC][DV];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int c = 0; c < DV; ++c) o[h][c] = 0.f;
+    }
+
+    uint32_t cnt = 0;
+    bool ok = true;
+    for (int t = t_begin; t < t_end; ++t, ++cnt) {
+        const int st = cnt % NSTG;
+        ok = mbar_wait(&full_bar[st], (cnt / NSTG) & 1, wc, ST_DECODE_CONSUMER);
+        if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* ks = ring + st * C::STAGE_BYTES;
+        const uint8_t* vs = ks + C::TILE_BYTES;
+
+        // ---- scores of keys r0 = 16 warp + kq and r0 + 8 for every head
+        float s[2][GC];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int r = warp * 16 + kq + rr * 8;
+#pragma unroll
+            for (int h = 0; h < GC; ++h) s[rr][h] = 0.f;
+#pragma unroll
+            for (int c8 = 0; c8 < DQ / 8; ++c8) {
+                const int dim = dq * DQ + c8 * 8;             // first of 8 dims
+                const int slab = dim >> 6, chunk = (dim & 63) >> 3;
+                const uint4 w = *reinterpret_cast<const uint4*>(ks + slab * C::SLAB + swz(r, chunk));
+                const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
+                                     bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+#pragma unroll
+                for (int h = 0; h < GC; ++h)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) s[rr][h] = fmaf(qv[h][c8 * 8 + i], kf[i], s[rr][h]);
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int h = 0; h < GC; ++h) {
+                s[rr][h] += __shfl_xor_sync(0xffffffffu, s[rr][h], 1);
+                s[rr][h] += __shfl_xor_sync(0xffffffffu, s[rr][h], 2);
+            }
+        // ---- logits (base 2), mask, running max per head
+        float mt[GC];
+#pragma unroll
+        for (int h = 0; h < GC; ++h) mt[h] = -INFINITY;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int kj = t * TILE + warp * 16 + kq + rr * 8;
+#pragma unroll
+            for (int h = 0; h < GC; ++h) {
+                float x = s[rr][h];
+                if (SOFTCAP) x = p.softcap * LOG2E * tanhf(x / p.softcap);
+                if (ALIBI) x = fmaf(slope_l2[h], (float)kj, x);
+                if (kj >= p.Sk) x = -INFINITY;
+                s[rr][h] = x;
+                mt[h] = fmaxf(mt[h], x);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 4));
+            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 8));
+            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 16));
+        }
+        float pj[2][GC];
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            const float m_new = fmaxf(m[h], mt[h]);
+            const float alpha = (m[h] == -INFINITY) ? 0.f : ex2_approx(m[h] - m_new);
+            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+            pj[0][h] = ex2_approx(s[0][h] - m_ref);
+            pj[1][h] = ex2_approx(s[1][h] - m_ref);
+            if (m_new != -INFINITY) {
+                l[h] = l[h] * alpha + (pj[0][h] + pj[1][h]);
+#pragma unroll
+                for (int c = 0; c < DV; ++c) o[h][c] *= alpha;
+                m[h] = m_new;
+            }
+        }
+        if (dq == 0) {
+#pragma unroll
+            for (int h = 0; h < GC; ++h) {
+                p_s[warp][kq][h] = pj[0][h];
+                p_s[warp][kq + 8][h] = pj[1][h];
+            }
+        }
+        __syncwarp();
+        // ---- P V over the warp's 16 keys; lane owns dims [lane*DV, lane*DV + DV)
+        {
+            const int dim = lane * DV;
+            const int slab = dim >> 6, chunk = (dim & 63) >> 3, within = (dim & 7) * 2;  // bytes
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                const int r = warp * 16 + j;
+                const uint8_t* vp = vs + slab * C::SLAB + swz(r, chunk) + within;
+                float vf[DV];
+                if (DV == 4) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(vp);
+                    vf[0] = bf16lo(w.x);
+                    vf[1] = bf16hi(w.x);
+                    vf[2] = bf16lo(w.y);
+                    vf[3] = bf16hi(w.y);
+                } else {
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
+                    vf[0] = bf16lo(w);
+                    vf[1] = bf16hi(w);
+                }
+                float pr[GC];
+#pragma unroll
+                for (int h = 0; h < GC; h += 4) {
+                    if (GC - h >= 4) {
+                        const float4 t4 = *reinterpret_cast<const float4*>(&p_s[warp][j][h]);
+                        pr[h] = t4.x;
+                        pr[h + 1] = t4.y;
+                        pr[h + 2] = t4.z;
+                        pr[h + 3] = t4.w;
+                    } else {
+                        for (int i = h; i < GC; ++i) pr[i] = p_s[warp][j][i];
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < GC; ++h)
+#pragma unroll
+                    for (int c = 0; c < DV; ++c) o[h][c] = fmaf(pr[h], vf[c], o[h][c]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
+    }
+
+    // ---- merge the four warps' states (fixed order), then write
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 4);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
+        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            red_m[warp][h] = m[h];
+            red_l[warp][h] = l[h];
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < GC; ++h)
+#pragma unroll
+        for (int c = 0; c < DV; ++c) red_o[warp][h][lane * DV + c] = o[h][c];
+    asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
+    if (!ok || abort_flag) return;
+
+    const int tid = threadIdx.x;  // 0 .. 127
+    for (int i = tid; i < n_heads * D; i += CONSUMERS * 32) {
+        const int h = i / D, d = i % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < CONSUMERS; ++w) M = fmaxf(M, red_m[w][h]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < CONSUMERS; ++w) {
+                const float f = (red_m[w][h] == -INFINITY) ? 0.f : ex2_approx(red_m[w][h] - M);
+                L += red_l[w][h] * f;
+                O += red_o[w][h][d] * f;
+            }
+        }
+        const float val = (L > 0.f) ? O / L : 0.f;
+        const float lse2 = (L > 0.f) ? M + log2f(L) : -INFINITY;  // base 2
+        const int head = h0 + h;
+        const size_t row = (size_t)b * p.Hq + head;
+        if (p.num_splits == 1) {
+            p.out[row * D + d] = __float2bfloat16_rn(val);
+            if (p.lse && d == 0) p.lse[row] = lse2 * LN2;
+        } else {
+            const size_t prow = row * p.num_splits + split;
+            p.ws_o[prow * D + d] = val;
+            if (d == 0) p.ws_lse[prow] = lse2;
+        }
+    }
+}
+
+// Combine: one block per (b, h) row, one thread per output dimension.
+template <int D>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ ws_o,
+                                                           const float* __restrict__ ws_lse,
+                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                           int num_splits, float lse_to_natural) {
+    const size_t row = blockIdx.x;
+    const int d = threadIdx.x;
+    const float* ls = ws_lse + row * num_splits;
+    float M = -INFINITY;
+    for (int s = 0; s < num_splits; ++s) M = fmaxf(M, ls[s]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < num_splits; ++s) {
+            const float w = (ls[s] == -INFINITY) ? 0.f : ex2_approx(ls[s] - M);
+            L += w;
+            O += w * ws_o[(row * num_splits + s) * D + d];
+        }
+    }
+    out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    if (lse && d == 0) lse[row] = (L > 0.f) ? (M + log2f(L)) * lse_to_natural : -INFINITY;
+}
+
+template <int D, int GC, bool SOFTCAP, bool ALIBI>
+cudaError_t launch_dec(const DecParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    auto kern = decode_bf16_kernel<D, GC, SOFTCAP, ALIBI>;
+    const int smem = DCfg<D>::SMEM;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const long long grid = (long long)p.B * p.Hkv * p.n_chunks * p.num_splits;
+    kern<<<(unsigned)grid, DEC_THREADS, smem, stream>>>(tk, tv, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || p.num_splits == 1) return e;
+    // every partial lse is in base 2 (logits carry the log2(e) factor).
+    decode_combine_kernel<D><<<p.B * p.Hq, D, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits, LN2);
+    return cudaGetLastError();
+}
+
+template <int D, int GC>
+cudaError_t launch_dec_flags(const DecParams& p, bool cap, bool ali, const CUtensorMap& tk, const CUtensorMap& tv,
+                             cudaStream_t s) {
+    if (cap) return ali ? launch_dec<D, GC, true, true>(p, tk, tv, s) : launch_dec<D, GC, true, false>(p, tk, tv, s);
+    return ali ? launch_dec<D, GC, false, true>(p, tk, tv, s) : launch_dec<D, GC, false, false>(p, tk, tv, s);
+}
+
+}  // namespace
+
+void decode_split_plan(int B, int Hkv, int Sk, int num_sms, int requested, int* num_splits, int* chunk) {
+    const int tiles = (Sk + TILE - 1) / TILE;
+    int s_best = 1;
+    if (requested > 0) {
+        s_best = requested < tiles ? requested : tiles;
+    } else {
+        // Pick the split count whose waves of resident CTAs waste the least
+        // time: minimise ceil(rows * s / slots) * ceil(tiles / s).
+        const long long rows = (long long)B * Hkv;
+        const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * 2;
+        long long best = -1;
+        for (int s = 1; s <= tiles && s <= 256; ++s) {
+            const int ct = (tiles + s - 1) / s;
+            if ((tiles + ct - 1) / ct != s) continue;  // same chunking as a smaller s
+            const long long waves = (rows * s + slots - 1) / slots;
+            const long long cost = waves * ct * 64 + s;  // small bias towards fewer splits
+            if (best < 0 || cost < best) {
+                best = cost;
+                s_best = s;
+            }
+        }
+    }
+    const int ct = (tiles + s_best - 1) / s_best;
+    *num_splits = (tiles + ct - 1) / ct;
+    *chunk = ct * TILE;
+}
+
+cudaError_t launch_decode_bf16(const DecodeProblem& f, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t stream) {
+    DecParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(f.q);
+    p.out = static_cast<__nv_bfloat16*>(f.out);
+    p.lse = f.lse;
+    p.slopes = f.slopes;
+    p.ws_o = f.ws_o;
+    p.ws_lse = f.ws_lse;
+    p.status = f.status;
+    p.timeout_ns = f.timeout_ns;
+    p.B = f.B;
+    p.Hq = f.Hq;
+    p.Hkv = f.Hkv;
+    p.Sk = f.Sk;
+    p.G = f.Hq / f.Hkv;
+    p.num_splits = f.num_splits;
+    p.chunk_tiles = f.chunk / TILE;
+    p.n_tiles = (f.Sk + TILE - 1) / TILE;
+    p.softcap = f.softcap;
+    const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
+    p.qscale = cap ? f.scale : f.scale * LOG2E;
+    const int G = p.G;
+    if (f.D == 128) {
+        const int GC = G >= 4 ? 4 : (G == 3 ? 4 : (G == 2 ? 2 : 1));
+        p.n_chunks = (G + GC - 1) / GC;
+        if (GC == 4) return launch_dec_flags<128, 4>(p, cap, ali, tk, tv, stream);
+        if (GC == 2) return launch_dec_flags<128, 2>(p, cap, ali, tk, tv, stream);
+        return launch_dec_flags<128, 1>(p, cap, ali, tk, tv, stream);
+    }
+    const int GC = G >= 5 ? 8 : (G >= 3 ? 4 : (G == 2 ? 2 : 1));
+    p.n_chunks = (G + GC - 1) / GC;
+    if (GC == 8) return launch_dec_flags<64, 8>(p, cap, ali, tk, tv, stream);
+    if (GC == 4) return launch_dec_flags<64, 4>(p, cap, ali, tk, tv, stream);
+    if (GC == 2) return launch_dec_flags<64, 2>(p, cap, ali, tk, tv, stream);
+    return launch_dec_flags<64, 1>(p, cap, ali, tk, tv, stream);
+}
+
+}  // namespace gbattn

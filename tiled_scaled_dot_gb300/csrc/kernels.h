@@ -1,0 +1,75 @@
+// kernels.h -- internal interface between the C ABI layer (api.cu) and the
+// kernel translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gbattn {
+
+// A validated forward problem (sizes checked, pointers non-null where required).
+struct FwdProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* slopes;        // [Hq] or nullptr
+    const int32_t* row_bounds;  // [B, Sq, 2] or nullptr
+    void* out;
+    float* lse;                 // [B, Hq, Sq] or nullptr
+    int B, Hq, Hkv, Sq, Sk, D;
+    float scale;
+    int causal;
+    int wl, wr;                 // -1 = unbounded
+    float softcap;              // 0 = none
+    unsigned int* status;       // device status word
+    unsigned long long timeout_ns;
+    int num_sms;
+};
+
+struct DecodeProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* slopes;
+    void* out;
+    float* lse;
+    int B, Hq, Hkv, Sk, D;
+    float scale;
+    float softcap;
+    int num_splits;             // resolved (>= 1)
+    int chunk;                  // keys per split, multiple of 64
+    float* ws_o;                // [B, Hq, num_splits, D] fp32 (num_splits > 1)
+    float* ws_lse;              // [B, Hq, num_splits] fp32 (num_splits > 1)
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    int num_sms;
+};
+
+// Bits of the device status word: which wait gave up.
+enum : unsigned int {
+    ST_PREFILL_PRODUCER = 1u << 0,
+    ST_PREFILL_MMA = 1u << 1,
+    ST_PREFILL_SOFTMAX = 1u << 2,
+    ST_PREFILL_EPILOGUE = 1u << 3,
+    ST_DECODE_PRODUCER = 1u << 8,
+    ST_DECODE_CONSUMER = 1u << 9,
+    ST_DIAG = 1u << 16,
+};
+
+// 3-D bf16 tensor map over a contiguous [planes][rows][cols] array with
+// a {64, box_rows, 1} box and 128-byte swizzle; out-of-range rows read as 0.
+bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
+                        uint32_t box_rows);
+
+// Kernel launchers.  Each returns the launch's cudaError_t.
+cudaError_t launch_prefill_bf16(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, cudaStream_t stream);
+cudaError_t launch_prefill_f32(const FwdProblem& p, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
+                               cudaStream_t stream);
+
+// Decode split choice shared by attn_decode and attn_decode_workspace_size.
+void decode_split_plan(int B, int Hkv, int Sk, int num_sms, int requested, int* num_splits, int* chunk);
+
+}  // namespace gbattn
