@@ -53,7 +53,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
-    ap.add_argument("--profile", action="store_true", help="kernel launches only (for an ncu launch list)")
+    ap.add_argument("--profile", choices=["prefill", "decode", "both"], default=None,
+                    help="launch warm-up + steps of one path and exit (for ncu); no timing, one input copy")
+    ap.add_argument("--decode-b", type=int, default=None, help="override the decode batch (smaller ncu captures)")
     return ap.parse_args()
 
 
@@ -185,7 +187,7 @@ def bench_prefill(g, w, args, ws, dev, pk):
     stream = torch.cuda.current_stream()
     base = make_inputs(w, dev)
     in_bytes = sum(t.numel() * t.element_size() for k, t in base.items() if k in ("q", "k", "v"))
-    n_copies = max(1, math.ceil(2 * L2_BYTES / in_bytes))  # rotate so no step reads another's data from L2
+    n_copies = 1 if args.profile else max(1, math.ceil(2 * L2_BYTES / in_bytes))  # rotate past L2
     sets = [base] + [{k: (None if t is None else t.clone()) for k, t in base.items()} for _ in range(n_copies - 1)]
     outs = [torch.empty_like(base["q"]) for _ in range(n_copies)]
     fn = lambda i: prefill_call(g, w, sets[i % n_copies], outs[i % n_copies])
@@ -240,6 +242,9 @@ def e2e_prefill(g, w, base, args, ws, stream, flops):
 
 def bench_decode(g, args, ws, dev, pk):
     w = WORKLOADS[DECODE]
+    if args.decode_b:
+        from synth.workloads import scaled
+        w = scaled(w, B=args.decode_b)
     stream = torch.cuda.current_stream()
     x = make_inputs(w, dev)
     out = torch.empty_like(x["q"])
@@ -327,7 +332,7 @@ def oracle_rows(w, x_cpu, seconds, seed=11):
         dt = time.time() - t0
         if dt >= seconds or n >= total_rows:
             return rows, dt
-        n = min(total_rows, int(n * max(1.2, min(16.0, 1.05 * seconds / max(dt, 1e-3))))))
+        n = min(total_rows, int(n * max(1.2, min(16.0, 1.05 * seconds / max(dt, 1e-3)))))
 
 
 def oracle_sample(w, x_cpu, seconds):
@@ -358,19 +363,23 @@ def main():
     pk = peaks()
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else dev.index
+    if args.profile:
+        if args.profile in ("prefill", "both"):
+            bench_prefill(g, w, args, ws, dev, pk)
+        if args.profile in ("decode", "both"):
+            bench_decode(g, args, ws, dev, pk)
+        if g.device_status() != 0:
+            raise RuntimeError("device status word set")
+        if rank == 0:
+            print(json.dumps({"profile_run": args.profile, "workload": w.name}))
+        return
     sampler = ClockSampler(gpu_index)
     sampler.start()
     try:
         pre = bench_prefill(g, w, args, ws, dev, pk)
-        dec = None if (args.no_decode or args.profile) else bench_decode(g, args, ws, dev, pk)
-        if args.profile:
-            dec = bench_decode(g, args, ws, dev, pk) if not args.no_decode else None
+        dec = None if args.no_decode else bench_decode(g, args, ws, dev, pk)
     finally:
         clocks = sampler.stop()
-    if args.profile:
-        if rank == 0:
-            print(json.dumps({"profile_run": True, "workload": w.name}))
-        return
     if g.device_status() != 0:
         raise RuntimeError("device status word set during the benchmark")
     total_tf = pre["tflops_per_gpu"] * ws
