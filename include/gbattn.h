@@ -150,6 +150,30 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
                 int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap, int num_splits,
                 void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
+/*
+ * attn_decode_noalloc -- attn_decode without a caller-provided workspace.
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that cannot allocate device memory themselves (an engine whose own pool owns
+ * all device memory, or a latency-critical loop that must not call cudaMalloc,
+ * which can synchronise the device).  Same arguments and results as
+ * attn_decode, minus workspace / workspace_bytes.
+ *
+ * The split partials go to a fixed scratch array of GBATTN_NOALLOC_SCRATCH_BYTES
+ * that the library keeps in device memory on every GPU that loads it, until
+ * the process exits.  Nothing is allocated by this call.  A problem whose
+ * workspace (attn_decode_workspace_size) exceeds that size returns
+ * GBATTN_ERR_UNSUPPORTED; use attn_decode with your own workspace then.
+ * All calls share the one array and it keeps the last call's contents, so
+ * calls that overlap on the GPU (different streams or host threads) race;
+ * serialise them.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture begins.
+ */
+#define GBATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int attn_decode_noalloc(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out,
+                        float* lse_out, int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap,
+                        int num_splits, int dtype, void* stream);
+
 /* Human-readable text of a status code (static storage). */
 const char* gbattn_status_string(int status);
 

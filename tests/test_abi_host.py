@@ -25,6 +25,7 @@ def _declared_functions():
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"^\s*#[^\n]*", "", text, flags=re.M)  # preprocessor lines
         for m in re.finditer(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\(([^;{}]*)\)\s*;", text):
             names.append(m.group(1))
     return names
