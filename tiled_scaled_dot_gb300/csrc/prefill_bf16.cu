@@ -6,36 +6,39 @@
 // attention.fkc.md, attention_naive: scale, softcap, ALiBi, causal / window /
 // per-row mask, GQA, fully-masked row -> zeros.
 //
-// Structure (one persistent CTA per SM, 12 warps in three warpgroups):
-//   warps 0-3  softmax for query slot 0 (thread r owns query row r = TMEM lane r)
-//   warps 4-7  softmax for query slot 1
-//   warp  8    TMA producer: Q tiles once per item, K/V tiles through an
-//              NS-stage shared-memory ring (128-byte swizzle)
-//   warp  9    MMA issuer (one thread): S = Q K^T (both operands from shared
-//              memory) and O += P V (P from TMEM, V from shared memory),
-//              fp32 accumulators in TMEM
-//   warps 10-11 idle
-// The control warpgroup gives registers to the softmax warpgroups
-// (setmaxnreg): 2 x 128 x SOFTMAX_REGS + 128 x CONTROL_REGS must not exceed
-// the launch allocation of 384 x LAUNCH_REGS, which the host checks.
-// Two query slots ping-pong on the tensor core: while softmax works on slot 0's
-// scores the MMA thread runs slot 1's P V and its next Q K^T, and vice versa.
-// A work item is two 128-row query tiles that share one K/V stream: two heads of
-// one GQA group at the same rows (Hq / Hkv even), or two consecutive row tiles of
-// one head (otherwise).  Items are dealt to CTAs heaviest first in a
-// boustrophedon order, so causal work evens out.
+// Structure (one persistent CTA per SM, 16 warps in four warpgroups):
+//   WG0 (warps 0-3)    softmax for query slot 0: thread r owns query row r,
+//                      which is TMEM lane r of the slot's S and O tiles
+//   WG1 (warps 4-7)    softmax for query slot 1
+//   WG2 (warps 8-11)   epilogue for both slots: O / l -> bf16 rows, lse
+//   WG3 warp 12        TMA producer: Q tiles once per item, K/V tiles through
+//                      an NS-stage shared-memory ring (128-byte swizzle)
+//   WG3 warp 13        MMA issuer (one thread): S = Q K^T with both operands in
+//                      shared memory, O += P V with P in TMEM and V in shared
+//                      memory, fp32 accumulators in TMEM
+//   WG3 warps 14-15    idle
+// Registers move to the softmax warpgroups with setmaxnreg:
+// 2 x 128 x SOFTMAX_REGS + 128 x (EPI_REGS + CONTROL_REGS) <= 512 x LAUNCH_REGS,
+// and the host refuses to launch if the compiled launch allocation is smaller.
+//
+// Two query slots ping-pong on the tensor core: while softmax works on one
+// slot's scores, the MMA thread runs the other slot's P V and next Q K^T.  A
+// work item is two 128-row query tiles that share one K/V stream: two heads of
+// one GQA group at the same rows (Hq / Hkv even), or two consecutive row tiles
+// of one head (otherwise).  Items are dealt to CTAs heaviest first in a
+// boustrophedon order, so causal work evens out across SMs.
 //
 // TMEM columns (512 allocated): S/P of slot x at 128 x, O of slot x at
 // 256 + D x.  P (bf16, two per 32-bit column) overwrites the first 64 columns of
 // its S tile; the next Q K^T into that tile is issued after the P V that reads
-// it, and tcgen05 operations of one thread execute in order.
+// it, and tcgen05 operations issued by one thread execute in order.
 //
 // Causal and window tile skipping ("gfx942 unified attention", section 4): a
 // slot visits only the key tiles that intersect the union of its rows'
 // admissible ranges; element masks are applied only on tiles that cut a row's
 // range.  Lazy rescaling: O and l are rescaled only when the running max grows
-// by more than 8 (base-2 units); the stale max is used as the reference
-// otherwise, which keeps every p <= 2^8 and leaves o / l exact.
+// by more than 8 (base-2 units); otherwise the stale max stays the reference,
+// which keeps every p <= 2^8 and leaves o / l exact.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -46,17 +49,19 @@ namespace {
 
 constexpr int BM = 128;  // query rows per slot
 constexpr int BN = 128;  // keys per K/V tile
-constexpr int NUM_WARPS = 12;
+constexpr int NUM_WARPS = 16;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
-constexpr int WARP_PRODUCER = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_PRODUCER = 12;
+constexpr int WARP_MMA = 13;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // base-2 units
-constexpr int LAUNCH_REGS = 168;          // 65536 / 384, rounded down to a multiple of 8
-constexpr int SOFTMAX_REGS = 208;
-constexpr int CONTROL_REGS = 88;
-static_assert(2 * 128 * SOFTMAX_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS, "register split");
+constexpr int LAUNCH_REGS = 128;          // 65536 / 512
+constexpr int SOFTMAX_REGS = 184;
+constexpr int EPI_REGS = 64;
+constexpr int CONTROL_REGS = 80;
+static_assert(2 * 128 * SOFTMAX_REGS + 128 * EPI_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS,
+              "register split");
 
 template <int D>
 struct Cfg {
@@ -80,7 +85,7 @@ struct Params {
     int B, Hq, Hkv, Sq, Sk, G;
     int causal, wl, wr;
     float scale_log2;  // softmax_scale * log2(e)
-    float cap_in;      // softmax_scale / softcap
+    float cap_e2;      // 2 * softmax_scale / softcap * log2(e): 2^(s cap_e2) = e^(2 scale s / c)
     float cap_out;     // softcap * log2(e)
     int n_qt;          // query tiles per head
     int pair_heads;    // 1: slots are heads (2p, 2p+1) at one row tile; 0: row tiles (2t, 2t+1) of one head
@@ -92,7 +97,7 @@ struct Slot {
     int lo, hi;   // key-tile range, lo > hi: no admissible key for any row
 };
 
-// Admissible key interval [a, b] of query row qi (a > b when empty).
+// Admissible key interval [a, e] of query row qi (a > e when empty).
 __device__ __forceinline__ void row_interval(const Params& p, int b, int qi, int& a, int& e) {
     a = 0;
     e = p.Sk - 1;
@@ -160,14 +165,212 @@ __device__ __forceinline__ int item_of(int k, int cta, int grid) {
 __device__ __forceinline__ bool slot_live(const Slot& s) { return s.t >= 0 && s.lo <= s.hi; }
 __device__ __forceinline__ bool in_range(const Slot& s, int u) { return s.t >= 0 && u >= s.lo && u <= s.hi; }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 struct Smem {
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], l_full[2];
     uint64_t kv_full[8], kv_empty[8];
     uint64_t drain;
+    float l_buf[2][2][BM];  // [item parity][slot][row]: softmax denominator l
+    float m_buf[2][2][BM];  // running max (base 2) for lse
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// ---------------------------------------------------------------------------- softmax role
+template <int D, bool SOFTCAP, bool ALIBI>
+__device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t tmem, const WaitCtl& wc,
+                                             int warp) {
+    using C = Cfg<D>;
+    const int x = warp >> 2;
+    const int r = threadIdx.x & (BM - 1);
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 128u * x;
+    const uint32_t tO = tmem + lane_off + C::O_COL + D * x;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    uint32_t s_cnt = 0, l_cnt = 0;
+    const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+    for (int k = 0;; ++k) {
+        const int item = item_of(k, cta, grid);
+        if (item >= p.n_items) break;
+        Slot s[2];
+        decode_item(p, item, s);
+        const Slot sl = s[x];
+        if (!slot_live(sl)) continue;  // unused or fully-masked tile: the epilogue writes zeros
+        const int qi = sl.t * BM + r;
+        int ra = 1, rb = 0;
+        if (qi < p.Sq) row_interval(p, sl.b, qi, ra, rb);
+        float slope_l2 = 0.f;
+        if (ALIBI) slope_l2 = __ldg(p.slopes + sl.h) * LOG2E;
+        float m_used = -INFINITY, l = 0.f;
+        for (int u = sl.lo; u <= sl.hi; ++u) {
+            const bool ok = mbar_wait(&sm.s_full[x], s_cnt & 1, wc, ST_PREFILL_SOFTMAX);
+            ++s_cnt;
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            float sv[BN];
+            tmem_ld64(tS, *reinterpret_cast<float(*)[64]>(&sv[0]));
+            tmem_ld64(tS + 64, *reinterpret_cast<float(*)[64]>(&sv[64]));
+            const int k0 = u * BN;
+            if (SOFTCAP || ALIBI) {
+                // base-2 logits: cap * tanh(scale s / cap) [+ slope (kj - qi)], times log2(e);
+                // tanh(y) = 1 - 2 / (e^{2y} + 1)
+#pragma unroll
+                for (int j = 0; j < BN; ++j) {
+                    float t;
+                    if (SOFTCAP) {
+                        const float e = ex2_approx(sv[j] * p.cap_e2);
+                        t = fmaf(-2.f * p.cap_out, rcp_approx(e + 1.f), p.cap_out);
+                    } else {
+                        t = sv[j] * p.scale_log2;
+                    }
+                    if (ALIBI) t = fmaf(slope_l2, (float)(k0 + j - qi), t);
+                    sv[j] = t;
+                }
+            }
+            if (k0 < ra || k0 + BN - 1 > rb) {
+#pragma unroll
+                for (int j = 0; j < BN; ++j) {
+                    const int kj = k0 + j;
+                    sv[j] = (kj < ra || kj > rb) ? -INFINITY : sv[j];
+                }
+            }
+            // row max over the tile: 8 independent chains of three-input max
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = max3(sv[i], sv[8 + i], sv[16 + i]);
+#pragma unroll
+            for (int j = 24; j + 16 <= BN; j += 16) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx[i] = max3(mx[i], sv[j + i], sv[j + 8 + i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], sv[BN - 8 + i]);
+            float m_tile = max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+            if (!(SOFTCAP || ALIBI)) m_tile *= p.scale_log2;  // scale > 0: max commutes with scaling
+            const float m_new = fmaxf(m_used, m_tile);
+            float alpha = 1.f;
+            if (m_new > m_used + RESCALE_THRESHOLD) {
+                if (m_used != -INFINITY) alpha = ex2_approx(m_used - m_new);
+                m_used = m_new;
+            }
+            const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+            const float2 nm = make_float2(-m_ref, -m_ref);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
+            uint32_t pw[BN / 2];
+#pragma unroll
+            for (int j = 0; j < BN; j += 2) {
+                float2 y = make_float2(sv[j], sv[j + 1]);
+                y = (SOFTCAP || ALIBI) ? __fadd2_rn(y, nm) : __ffma2_rn(y, sl2, nm);
+                const float2 pp = make_float2(ex2_approx(y.x), ex2_approx(y.y));
+                acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], pp);
+                pw[j >> 1] = pack_bf16x2(pp.x, pp.y);
+            }
+            const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
+            const float2 a = __fadd2_rn(a01, a23);
+            l = fmaf(l, alpha, a.x + a.y);
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
+            // Rescale O when any row of the warp moved its reference max.  The
+            // P V of the previous tile has completed: it was issued before this
+            // tile's Q K^T, whose completion we waited for.
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                for (int c = 0; c < D; c += 32) {
+                    float ov[32];
+                    tmem_ld32(tO + c, ov);
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(ov[i] * alpha);
+                    tmem_st32(tO + c, w);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm.p_full[x]);
+        }
+        // hand l and the reference max to the epilogue
+        const int par = l_cnt & 1;
+        sm.l_buf[par][x][r] = l;
+        sm.m_buf[par][x][r] = m_used;
+        ++l_cnt;
+        mbar_arrive(&sm.l_full[x]);
+    }
+}
+
+// ---------------------------------------------------------------------------- epilogue role
+template <int D>
+__device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_t tmem, const WaitCtl& wc,
+                                              int warp) {
+    using C = Cfg<D>;
+    const int r = threadIdx.x & (BM - 1);
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int grid = gridDim.x, cta = blockIdx.x;
+    uint32_t cnt[2] = {0, 0};
+    for (int k = 0;; ++k) {
+        const int item = item_of(k, cta, grid);
+        if (item >= p.n_items) break;
+        Slot s[2];
+        decode_item(p, item, s);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const Slot sl = s[x];
+            if (sl.t < 0) continue;
+            const int qi = sl.t * BM + r;
+            const bool live = qi < p.Sq;
+            const size_t row = ((size_t)sl.b * p.Hq + sl.h) * p.Sq + qi;
+            if (sl.lo > sl.hi) {
+                // No admissible key for any row of the tile: zero rows.
+                if (live) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
+#pragma unroll
+                    for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+                    if (p.lse) p.lse[row] = -INFINITY;
+                }
+                continue;
+            }
+            bool ok = mbar_wait(&sm.l_full[x], cnt[x] & 1, wc, ST_PREFILL_EPILOGUE);
+            ok = ok && mbar_wait(&sm.o_full[x], cnt[x] & 1, wc, ST_PREFILL_EPILOGUE);
+            const int par = cnt[x] & 1;
+            ++cnt[x];
+            if (!__all_sync(0xffffffffu, ok)) return;
+            tc_fence_after();
+            const float l = sm.l_buf[par][x][r];
+            const float m = sm.m_buf[par][x][r];
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            const uint32_t tO = tmem + lane_off + C::O_COL + D * x;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                float ov[32];
+                tmem_ld32(tO + c, ov);
+                if (live) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l);
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (live && p.lse) p.lse[row] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
+            tc_fence_before();
+            mbar_arrive(&sm.o_empty[x]);
+        }
+    }
+}
 
 template <int D, bool SOFTCAP, bool ALIBI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -185,6 +388,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
             mbar_init(&sm.q_full[x], 1);
             mbar_init(&sm.q_empty[x], 1);
@@ -192,6 +396,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&sm.p_full[x], BM);
             mbar_init(&sm.o_full[x], 1);
             mbar_init(&sm.o_empty[x], BM);
+            mbar_init(&sm.l_full[x], BM);
         }
         for (int i = 0; i < C::NS; ++i) {
             mbar_init(&sm.kv_full[i], 1);
@@ -210,312 +415,186 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     WaitCtl wc{&sm.abort_flag, p.status, p.timeout_ns};
-
     const int grid = gridDim.x, cta = blockIdx.x;
 
-    if (warp >= 8) {
     // Each warpgroup executes one setmaxnreg, at one program point, before its roles split.
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CONTROL_REGS));
-    if (warp == WARP_PRODUCER) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-        }
-        uint32_t kv_cnt = 0, q_cnt[2] = {0, 0};
-        bool ok = true;
-        for (int k = 0;; ++k) {
-            const int item = item_of(k, cta, grid);
-            if (item >= p.n_items) break;
-            Slot s[2];
-            decode_item(p, item, s);
+    if (warp < 8) {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
+        softmax_role<D, SOFTCAP, ALIBI>(p, sm, tmem, wc, warp);
+    } else if (warp < 12) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
+        epilogue_role<D>(p, sm, tmem, wc, warp);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CONTROL_REGS));
+        if (warp == WARP_PRODUCER) {
+            // -------------------------------------------------------- TMA producer
             if (lane == 0) {
-                const int hkv = s[0].h / p.G;
-                for (int x = 0; x < 2 && ok; ++x) {
-                    if (!slot_live(s[x])) continue;
-                    ok = mbar_wait(&sm.q_empty[x], (q_cnt[x] & 1) ^ 1, wc, ST_PREFILL_PRODUCER);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(&sm.q_full[x], C::Q_BYTES);
+                tma_prefetch_desc(&tmQ);
+                tma_prefetch_desc(&tmK);
+                tma_prefetch_desc(&tmV);
+            }
+            uint32_t kv_cnt = 0, q_cnt[2] = {0, 0};
+            bool ok = true;
+            for (int k = 0;; ++k) {
+                const int item = item_of(k, cta, grid);
+                if (item >= p.n_items) break;
+                Slot s[2];
+                decode_item(p, item, s);
+                if (lane == 0) {
+                    const int hkv = s[0].h / p.G;
 #pragma unroll
-                    for (int hf = 0; hf < C::HALVES; ++hf)
-                        tma_load_3d(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].t * BM,
-                                    s[x].b * p.Hq + s[x].h);
-                    ++q_cnt[x];
-                }
-                int ulo = 0x7fffffff, uhi = -1;
-                for (int x = 0; x < 2; ++x)
-                    if (slot_live(s[x])) {
-                        ulo = min(ulo, s[x].lo);
-                        uhi = max(uhi, s[x].hi);
-                    }
-                for (int u = ulo; u <= uhi && ok; ++u) {
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const int st = kv_cnt % C::NS;
-                        ok = mbar_wait(&sm.kv_empty[st], ((kv_cnt / C::NS) & 1) ^ 1, wc, ST_PREFILL_PRODUCER);
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        if (!slot_live(s[x])) continue;
+                        ok = mbar_wait(&sm.q_empty[x], (q_cnt[x] & 1) ^ 1, wc, ST_PREFILL_PRODUCER);
                         if (!ok) break;
-                        mbar_arrive_expect_tx(&sm.kv_full[st], C::KV_BYTES);
-                        uint8_t* dst = sKV + st * C::KV_BYTES;
+                        mbar_arrive_expect_tx(&sm.q_full[x], C::Q_BYTES);
 #pragma unroll
                         for (int hf = 0; hf < C::HALVES; ++hf)
-                            tma_load_3d(dst + hf * C::KV_SLAB, kv ? &tmV : &tmK, &sm.kv_full[st], hf * 64, u * BN,
-                                        s[0].b * p.Hkv + hkv);
-                        ++kv_cnt;
+                            tma_load_3d(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].t * BM,
+                                        s[x].b * p.Hq + s[x].h);
+                        ++q_cnt[x];
+                    }
+                    int ulo = 0x7fffffff, uhi = -1;
+#pragma unroll
+                    for (int x = 0; x < 2; ++x)
+                        if (slot_live(s[x])) {
+                            ulo = min(ulo, s[x].lo);
+                            uhi = max(uhi, s[x].hi);
+                        }
+                    for (int u = ulo; u <= uhi && ok; ++u) {
+#pragma unroll
+                        for (int kv = 0; kv < 2; ++kv) {
+                            const int st = kv_cnt % C::NS;
+                            ok = mbar_wait(&sm.kv_empty[st], ((kv_cnt / C::NS) & 1) ^ 1, wc, ST_PREFILL_PRODUCER);
+                            if (!ok) break;
+                            mbar_arrive_expect_tx(&sm.kv_full[st], C::KV_BYTES);
+                            uint8_t* dst = sKV + st * C::KV_BYTES;
+#pragma unroll
+                            for (int hf = 0; hf < C::HALVES; ++hf)
+                                tma_load_3d(dst + hf * C::KV_SLAB, kv ? &tmV : &tmK, &sm.kv_full[st], hf * 64,
+                                            u * BN, s[0].b * p.Hkv + hkv);
+                            ++kv_cnt;
+                        }
                     }
                 }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-        }
-        if (!ok && lane == 0) {
-            // Let the copies already issued land before the CTA leaves.
-            const uint32_t n = kv_cnt < (uint32_t)C::NS ? kv_cnt : (uint32_t)C::NS;
-            for (uint32_t i = kv_cnt - n; i < kv_cnt; ++i)
-                mbar_drain(&sm.kv_full[i % C::NS], (i / C::NS) & 1, 100000000ull);
-            for (int x = 0; x < 2; ++x)
-                if (q_cnt[x]) mbar_drain(&sm.q_full[x], (q_cnt[x] - 1) & 1, 100000000ull);
-        }
-    } else if (warp == WARP_MMA) {
-        // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
-        constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
-        uint32_t kv_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
-        bool ok = true;
-        const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
-        const uint32_t sKVa = smem_u32(sKV);
-        for (int k = 0;; ++k) {
-            const int item = item_of(k, cta, grid);
-            if (item >= p.n_items) break;
-            Slot s[2];
-            decode_item(p, item, s);
-            if (lane == 0) {
-                int ulo = 0x7fffffff, uhi = -1;
+            if (!ok && lane == 0) {
+                // Let the copies already issued land before the CTA leaves.
+                const uint32_t n = kv_cnt < (uint32_t)C::NS ? kv_cnt : (uint32_t)C::NS;
+                for (uint32_t i = kv_cnt - n; i < kv_cnt; ++i)
+                    mbar_drain(&sm.kv_full[i % C::NS], (i / C::NS) & 1, 100000000ull);
+#pragma unroll
                 for (int x = 0; x < 2; ++x)
-                    if (slot_live(s[x])) {
-                        ulo = min(ulo, s[x].lo);
-                        uhi = max(uhi, s[x].hi);
-                    }
-                bool q_ready[2] = {false, false};
-                auto issue_s = [&](int x, uint32_t kst) -> bool {
-                    if (!q_ready[x]) {
-                        if (!mbar_wait(&sm.q_full[x], q_cnt[x] & 1, wc, ST_PREFILL_MMA)) return false;
-                        ++q_cnt[x];
-                        q_ready[x] = true;
-                        tc_fence_after();
-                    }
-                    const uint32_t qa = sQa[x], ka = sKVa + kst * C::KV_BYTES;
+                    if (q_cnt[x]) mbar_drain(&sm.q_full[x], (q_cnt[x] - 1) & 1, 100000000ull);
+            }
+        } else if (warp == WARP_MMA) {
+            // -------------------------------------------------------- MMA issuer
+            constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
+            constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
+            uint32_t kv_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+            bool ok = true;
+            const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
+            const uint32_t sKVa = smem_u32(sKV);
+            for (int k = 0;; ++k) {
+                const int item = item_of(k, cta, grid);
+                if (item >= p.n_items) break;
+                Slot s[2];
+                decode_item(p, item, s);
+                if (lane == 0) {
+                    int ulo = 0x7fffffff, uhi = -1;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * C::Q_SLAB + (kk & 3) * 32;
-                        const uint32_t koff = (kk >> 2) * C::KV_SLAB + (kk & 3) * 32;
-                        umma_ss(tmem + 128u * x, sdesc_sw128(qa + off, 16), sdesc_sw128(ka + koff, 16), IDESC_S,
-                                kk > 0);
-                    }
-                    umma_commit(&sm.s_full[x]);
-                    return true;
-                };
-                if (ulo <= uhi) {
-                    // prologue: K of the first tile
-                    uint32_t kst = kv_cnt % C::NS;
-                    ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
-                    ++kv_cnt;
-                    if (ok) tc_fence_after();
-                    for (int x = 0; x < 2 && ok; ++x)
-                        if (in_range(s[x], ulo)) ok = issue_s(x, kst);
-                    if (ok) umma_commit(&sm.kv_empty[kst]);
-                    for (int u = ulo; u <= uhi && ok; ++u) {
-                        const uint32_t vst = kv_cnt % C::NS;
-                        ok = mbar_wait(&sm.kv_full[vst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
+                    for (int x = 0; x < 2; ++x)
+                        if (slot_live(s[x])) {
+                            ulo = min(ulo, s[x].lo);
+                            uhi = max(uhi, s[x].hi);
+                        }
+                    bool q_ready[2] = {false, false};
+                    auto issue_s = [&](int x, uint32_t kst) -> bool {
+                        if (!q_ready[x]) {
+                            if (!mbar_wait(&sm.q_full[x], q_cnt[x] & 1, wc, ST_PREFILL_MMA)) return false;
+                            ++q_cnt[x];
+                            q_ready[x] = true;
+                            tc_fence_after();
+                        }
+                        const uint32_t qlo = sdesc_lo(sQa[x], 16);
+                        const uint32_t klo = sdesc_lo(sKVa + kst * C::KV_BYTES, 16);
+                        const uint32_t dS = tmem + 128u * x;
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = ((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
+                            const uint32_t koff = ((kk >> 2) * C::KV_SLAB + (kk & 3) * 32) >> 4;
+                            umma_ss_lo(dS, qlo + off, klo + koff, IDESC_S, kk > 0);
+                        }
+                        umma_commit(&sm.s_full[x]);
+                        return true;
+                    };
+                    if (ulo <= uhi) {
+                        // prologue: K of the first tile
+                        uint32_t kst = kv_cnt % C::NS;
+                        ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
                         ++kv_cnt;
-                        if (!ok) break;
-                        tc_fence_after();
-                        const bool has_next = u < uhi;
-                        for (int x = 0; x < 2 && ok; ++x) {
-                            if (in_range(s[x], u)) {
-                                ok = mbar_wait(&sm.p_full[x], p_cnt[x] & 1, wc, ST_PREFILL_MMA);
-                                ++p_cnt[x];
-                                if (ok && u == s[x].lo) {
-                                    ok = mbar_wait(&sm.o_empty[x], (o_cnt[x] & 1) ^ 1, wc, ST_PREFILL_MMA);
-                                    ++o_cnt[x];
-                                }
-                                if (!ok) break;
-                                tc_fence_after();
-                                const uint32_t va = sKVa + vst * C::KV_BYTES;
+                        if (ok) tc_fence_after();
 #pragma unroll
-                                for (int kk = 0; kk < BN / 16; ++kk) {
-                                    umma_ts(tmem + C::O_COL + D * x, tmem + 128u * x + 8u * kk,
-                                            sdesc_sw128(va + kk * 16 * 128, C::KV_SLAB), IDESC_O,
-                                            (u > s[x].lo || kk > 0) ? 1u : 0u);
-                                }
-                                if (u == s[x].hi) umma_commit(&sm.o_full[x]);
-                            }
-                            if (has_next) {
-                                if (x == 0) {
-                                    kst = kv_cnt % C::NS;
-                                    ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
-                                    ++kv_cnt;
+                        for (int x = 0; x < 2 && ok; ++x)
+                            if (in_range(s[x], ulo)) ok = issue_s(x, kst);
+                        if (ok) umma_commit(&sm.kv_empty[kst]);
+                        for (int u = ulo; u <= uhi && ok; ++u) {
+                            const uint32_t vst = kv_cnt % C::NS;
+                            ok = mbar_wait(&sm.kv_full[vst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
+                            ++kv_cnt;
+                            if (!ok) break;
+                            tc_fence_after();
+                            const bool has_next = u < uhi;
+#pragma unroll
+                            for (int x = 0; x < 2 && ok; ++x) {
+                                if (in_range(s[x], u)) {
+                                    ok = mbar_wait(&sm.p_full[x], p_cnt[x] & 1, wc, ST_PREFILL_MMA);
+                                    ++p_cnt[x];
+                                    if (ok && u == s[x].lo) {
+                                        ok = mbar_wait(&sm.o_empty[x], (o_cnt[x] & 1) ^ 1, wc, ST_PREFILL_MMA);
+                                        ++o_cnt[x];
+                                    }
                                     if (!ok) break;
                                     tc_fence_after();
+                                    const uint32_t vlo = sdesc_lo(sKVa + vst * C::KV_BYTES, C::KV_SLAB);
+                                    const uint32_t dO = tmem + C::O_COL + D * x, aP = tmem + 128u * x;
+                                    const uint32_t acc0 = (u > s[x].lo) ? 1u : 0u;
+#pragma unroll
+                                    for (int kk = 0; kk < BN / 16; ++kk)
+                                        umma_ts_lo(dO, aP + 8u * kk, vlo + ((kk * 16 * 128) >> 4), IDESC_O,
+                                                   kk > 0 ? 1u : acc0);
+                                    if (u == s[x].hi) umma_commit(&sm.o_full[x]);
                                 }
-                                if (in_range(s[x], u + 1)) ok = issue_s(x, kst);
+                                if (has_next) {
+                                    if (x == 0) {
+                                        kst = kv_cnt % C::NS;
+                                        ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
+                                        ++kv_cnt;
+                                        if (!ok) break;
+                                        tc_fence_after();
+                                    }
+                                    if (in_range(s[x], u + 1)) ok = issue_s(x, kst);
+                                }
                             }
+                            if (!ok) break;
+                            umma_commit(&sm.kv_empty[vst]);
+                            if (has_next) umma_commit(&sm.kv_empty[kst]);
                         }
-                        if (!ok) break;
-                        umma_commit(&sm.kv_empty[vst]);
-                        if (has_next) umma_commit(&sm.kv_empty[kst]);
-                    }
-                    for (int x = 0; x < 2 && ok; ++x)
-                        if (slot_live(s[x])) umma_commit(&sm.q_empty[x]);
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-        }
-        if (lane == 0) {
-            // Every MMA issued must finish before TMEM is released.
-            umma_commit(&sm.drain);
-            mbar_drain(&sm.drain, 0, 100000000ull);
-        }
-    }
-    } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
-        // ------------------------------------------------------------ softmax / epilogue
-        const int x = warp >> 2;
-        const int r = threadIdx.x & (BM - 1);
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_off + 128u * x;
-        const uint32_t tO = tmem + lane_off + C::O_COL + D * x;
-        uint32_t s_cnt = 0, o_cnt = 0;
-        bool ok = true;
-        for (int k = 0; ok; ++k) {
-            const int item = item_of(k, cta, grid);
-            if (item >= p.n_items) break;
-            Slot s[2];
-            decode_item(p, item, s);
-            const Slot sl = s[x];
-            if (sl.t < 0) continue;
-            const int qi = sl.t * BM + r;
-            const bool live = qi < p.Sq;
-            int ra = 1, rb = 0;
-            if (live) row_interval(p, sl.b, qi, ra, rb);
-            const size_t row = ((size_t)sl.b * p.Hq + sl.h) * p.Sq + qi;
-            if (sl.lo > sl.hi) {
-                // No admissible key for any row of this tile: zero rows.
-                if (live) {
-                    uint4 z = make_uint4(0, 0, 0, 0);
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
 #pragma unroll
-                    for (int i = 0; i < D / 8; ++i) dst[i] = z;
-                    if (p.lse) p.lse[row] = -INFINITY;
-                }
-                continue;
-            }
-            float slope_l2 = 0.f;
-            if (ALIBI) slope_l2 = __ldg(p.slopes + sl.h) * LOG2E;
-            float m_used = -INFINITY, l = 0.f;
-            for (int u = sl.lo; u <= sl.hi; ++u) {
-                ok = mbar_wait(&sm.s_full[x], s_cnt & 1, wc, ST_PREFILL_SOFTMAX);
-                ++s_cnt;
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float sv[BN];
-                tmem_ld64(tS, *reinterpret_cast<float(*)[64]>(&sv[0]));
-                tmem_ld64(tS + 64, *reinterpret_cast<float(*)[64]>(&sv[64]));
-                const int k0 = u * BN;
-                // base-2 logits
-#pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    float t;
-                    if (SOFTCAP) {
-                        t = p.cap_out * tanhf(sv[j] * p.cap_in);
-                    } else {
-                        t = sv[j] * p.scale_log2;
-                    }
-                    if (ALIBI) t = fmaf(slope_l2, (float)(k0 + j - qi), t);
-                    sv[j] = t;
-                }
-                if (k0 < ra || k0 + BN - 1 > rb) {
-#pragma unroll
-                    for (int j = 0; j < BN; ++j) {
-                        const int kj = k0 + j;
-                        if (kj < ra || kj > rb) sv[j] = -INFINITY;
+                        for (int x = 0; x < 2 && ok; ++x)
+                            if (slot_live(s[x])) umma_commit(&sm.q_empty[x]);
                     }
                 }
-                float mx[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) mx[i] = sv[i];
-#pragma unroll
-                for (int j = 8; j < BN; ++j) mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
-                const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                const float m_new = fmaxf(m_used, m_tile);
-                float alpha = 1.f;
-                const bool grow = m_new > m_used + RESCALE_THRESHOLD;
-                if (grow) {
-                    if (m_used != -INFINITY) alpha = ex2_approx(m_used - m_new);
-                    m_used = m_new;
-                }
-                // O rescale (warp-collective TMEM traffic if any row of the warp needs it).
-                // A row's earlier P V completed before this tile's scores (in-order tcgen05).
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                    l *= alpha;
-#pragma unroll
-                    for (int c = 0; c < D; c += 32) {
-                        float ov[32];
-                        tmem_ld32(tO + c, ov);
-                        uint32_t w[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(ov[i] * alpha);
-                        tmem_st32(tO + c, w);
-                    }
-                }
-                const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-                float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                uint32_t pw[BN / 2];
-#pragma unroll
-                for (int j = 0; j < BN; j += 2) {
-                    const float p0 = ex2_approx(sv[j] - m_ref);
-                    const float p1 = ex2_approx(sv[j + 1] - m_ref);
-                    ls[(j >> 1) & 7] += p0 + p1;
-                    pw[j >> 1] = pack_bf16x2(p0, p1);
-                }
-                l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
-                tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&pw[0]));
-                tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&pw[32]));
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&sm.p_full[x]);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
             }
-            if (!ok) break;
-            // epilogue: O = o / l (zero row if l == 0), bf16, straight from registers.
-            ok = mbar_wait(&sm.o_full[x], o_cnt & 1, wc, ST_PREFILL_EPILOGUE);
-            ++o_cnt;
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
+            if (lane == 0) {
+                // Every MMA issued must finish before TMEM is released.
+                umma_commit(&sm.drain);
+                mbar_drain(&sm.drain, 0, 100000000ull);
             }
-            tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                float ov[32];
-                tmem_ld32(tO + c, ov);
-                if (live) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l);
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                }
-            }
-            if (live && p.lse) p.lse[row] = (l > 0.f) ? (m_used + log2f(l)) * LN2 : -INFINITY;
-            tc_fence_before();
-            mbar_arrive(&sm.o_empty[x]);
         }
     }
 
@@ -565,7 +644,7 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
     p.wl = f.wl;
     p.wr = f.wr;
     p.scale_log2 = f.scale * LOG2E;
-    p.cap_in = f.softcap > 0.f ? f.scale / f.softcap : 0.f;
+    p.cap_e2 = f.softcap > 0.f ? 2.f * f.scale / f.softcap * LOG2E : 0.f;
     p.cap_out = f.softcap * LOG2E;
     p.n_qt = (f.Sq + BM - 1) / BM;
     p.pair_heads = (p.G % 2 == 0) ? 1 : 0;
