@@ -511,7 +511,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             uhi = max(uhi, s[x].hi);
                         }
                     bool q_ready[2] = {false, false};
-                    auto issue_s = [&](int x, uint32_t kst) -> bool {
+                    // S_x(ut) = Q_x K_ut^T; after the slot's last tile Q_x is released
+                    // at once, so the next item's Q load overlaps this item's tail.
+                    auto issue_s = [&](int x, uint32_t kst, int ut) -> bool {
                         if (!q_ready[x]) {
                             if (!mbar_wait(&sm.q_full[x], q_cnt[x] & 1, wc, ST_PREFILL_MMA)) return false;
                             ++q_cnt[x];
@@ -528,6 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             umma_ss_lo(dS, qlo + off, klo + koff, IDESC_S, kk > 0);
                         }
                         umma_commit(&sm.s_full[x]);
+                        if (ut == s[x].hi) umma_commit(&sm.q_empty[x]);
                         return true;
                     };
                     if (ulo <= uhi) {
@@ -538,15 +541,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (ok) tc_fence_after();
 #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x)
-                            if (in_range(s[x], ulo)) ok = issue_s(x, kst);
+                            if (in_range(s[x], ulo)) ok = issue_s(x, kst, ulo);
                         if (ok) umma_commit(&sm.kv_empty[kst]);
                         for (int u = ulo; u <= uhi && ok; ++u) {
+                            // Wait for V_u and K_{u+1} up front, so that each slot's
+                            // P V and next Q K^T go to the tensor pipe as one run.
                             const uint32_t vst = kv_cnt % C::NS;
                             ok = mbar_wait(&sm.kv_full[vst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
                             ++kv_cnt;
                             if (!ok) break;
-                            tc_fence_after();
                             const bool has_next = u < uhi;
+                            if (has_next) {
+                                kst = kv_cnt % C::NS;
+                                ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
+                                ++kv_cnt;
+                                if (!ok) break;
+                            }
+                            tc_fence_after();
 #pragma unroll
                             for (int x = 0; x < 2 && ok; ++x) {
                                 if (in_range(s[x], u)) {
@@ -567,24 +578,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                    kk > 0 ? 1u : acc0);
                                     if (u == s[x].hi) umma_commit(&sm.o_full[x]);
                                 }
-                                if (has_next) {
-                                    if (x == 0) {
-                                        kst = kv_cnt % C::NS;
-                                        ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
-                                        ++kv_cnt;
-                                        if (!ok) break;
-                                        tc_fence_after();
-                                    }
-                                    if (in_range(s[x], u + 1)) ok = issue_s(x, kst);
-                                }
+                                if (has_next && in_range(s[x], u + 1)) ok = issue_s(x, kst, u + 1);
                             }
                             if (!ok) break;
                             umma_commit(&sm.kv_empty[vst]);
                             if (has_next) umma_commit(&sm.kv_empty[kst]);
                         }
-#pragma unroll
-                        for (int x = 0; x < 2 && ok; ++x)
-                            if (slot_live(s[x])) umma_commit(&sm.q_empty[x]);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
