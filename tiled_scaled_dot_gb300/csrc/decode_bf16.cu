@@ -15,9 +15,10 @@
 //     free of bank conflicts);
 //   * four consumer warps take 16 keys of each tile each and keep their own
 //     running (m, l, o) per head, merged once at the end of the split.
-// Scores: lane (key kq, quarter dq) dots D/4 dimensions and the quarters are
-// summed with two shuffles.  P V: lane owns D/32 output dimensions; the
-// probabilities reach it through a small per-warp shared buffer.
+// Scores: lane (key kq, dimension group dq) dots D/8 dimensions against every
+// head with packed FFMA2 and a shuffle reduce-scatter sums the groups.  P V:
+// lane owns D/32 output dimensions; probabilities reach it through a small
+// per-warp shared buffer.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -71,12 +72,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const DecParams p) {
     using C = DCfg<D>;
-    constexpr int DQ = D / 4;    // dims per lane in Q K^T
     constexpr int DV = D / 32;   // dims per lane in P V
     extern __shared__ __align__(1024) uint8_t dyn_smem[];
     __shared__ uint64_t full_bar[NSTG], empty_bar[NSTG];
     __shared__ int abort_flag;
-    __shared__ __align__(16) float p_s[CONSUMERS][16][GC < 4 ? 4 : GC];
+    __shared__ __align__(16) float2 p_s[CONSUMERS][16][GC];  // (p, p) per key and head
+    __shared__ __align__(16) float2 a_s[CONSUMERS][GC];      // (alpha, alpha) per head
     __shared__ float red_m[CONSUMERS][GC], red_l[CONSUMERS][GC];
     __shared__ __align__(16) float red_o[CONSUMERS][GC][D];
 
@@ -137,37 +138,43 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     }
 
     // -------------------------------------------------------------------- consumers
-    const int kq = lane >> 2, dq = lane & 3;
-    float qv[GC][DQ];
+    // Scores: lane = (key kq in 0..3, dimension group dq in 0..7).  A lane dots
+    // D/8 dimensions of one key against every head of the chunk (packed FFMA2),
+    // then a reduce-scatter over the 8 dimension-group lanes leaves one head's
+    // full score in each lane (head hsel, duplicated in the 8/GC lanes that
+    // differ only in dq's low bits).  P V: lane owns D/32 output dimensions of
+    // every head; probabilities and rescale factors reach it through shared memory.
+    constexpr int DQ = D / 8;
+    constexpr int DUP = 8 / GC;  // lanes holding the same head after the reduce-scatter
+    const int kq = lane >> 3, dq = lane & 7;
+    int hsel = 0;
+    if (GC >= 2) hsel += ((dq >> 2) & 1) * (GC / 2);
+    if (GC >= 4) hsel += ((dq >> 1) & 1) * (GC / 4);
+    if (GC >= 8) hsel += (dq & 1);
+    const bool writer = (dq & (DUP - 1)) == 0;
+
+    float2 q2[GC][DQ / 2];
 #pragma unroll
     for (int h = 0; h < GC; ++h) {
         const bool hv = h < n_heads;
         const __nv_bfloat16* qp = p.q + (size_t)(b * p.Hq + h0 + (hv ? h : 0)) * D + dq * DQ;
 #pragma unroll
         for (int d = 0; d < DQ; d += 8) {
-            uint4 w = hv ? *reinterpret_cast<const uint4*>(qp + d) : make_uint4(0, 0, 0, 0);
-            qv[h][d + 0] = bf16lo(w.x) * p.qscale;
-            qv[h][d + 1] = bf16hi(w.x) * p.qscale;
-            qv[h][d + 2] = bf16lo(w.y) * p.qscale;
-            qv[h][d + 3] = bf16hi(w.y) * p.qscale;
-            qv[h][d + 4] = bf16lo(w.z) * p.qscale;
-            qv[h][d + 5] = bf16hi(w.z) * p.qscale;
-            qv[h][d + 6] = bf16lo(w.w) * p.qscale;
-            qv[h][d + 7] = bf16hi(w.w) * p.qscale;
+            const uint4 w = hv ? *reinterpret_cast<const uint4*>(qp + d) : make_uint4(0, 0, 0, 0);
+            q2[h][d / 2 + 0] = make_float2(bf16lo(w.x) * p.qscale, bf16hi(w.x) * p.qscale);
+            q2[h][d / 2 + 1] = make_float2(bf16lo(w.y) * p.qscale, bf16hi(w.y) * p.qscale);
+            q2[h][d / 2 + 2] = make_float2(bf16lo(w.z) * p.qscale, bf16hi(w.z) * p.qscale);
+            q2[h][d / 2 + 3] = make_float2(bf16lo(w.w) * p.qscale, bf16hi(w.w) * p.qscale);
         }
     }
-    float slope_l2[GC];
-#pragma unroll
-    for (int h = 0; h < GC; ++h) slope_l2[h] = (ALIBI && h < n_heads) ? p.slopes[h0 + h] * LOG2E : 0.f;
+    const float slope_l2 = (ALIBI && hsel < n_heads) ? p.slopes[h0 + hsel] * LOG2E : 0.f;
 
-    float m[GC], l[GC], o[GC][DV];
+    float m_h = -INFINITY, l_h = 0.f;  // running max / partial sum of this lane's head and keys
+    float2 o2[GC][DV / 2];
 #pragma unroll
-    for (int h = 0; h < GC; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
+    for (int h = 0; h < GC; ++h)
 #pragma unroll
-        for (int c = 0; c < DV; ++c) o[h][c] = 0.f;
-    }
+        for (int c = 0; c < DV / 2; ++c) o2[h][c] = make_float2(0.f, 0.f);
 
     uint32_t cnt = 0;
     bool ok = true;
@@ -181,80 +188,93 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         const uint8_t* ks = ring + st * C::STAGE_BYTES;
         const uint8_t* vs = ks + C::TILE_BYTES;
 
-        // ---- scores of keys r0 = 16 warp + kq and r0 + 8 for every head
-        float s[2][GC];
+        // ---- scores: 4 passes of 4 keys, key r = 16 warp + 4 pass + kq
+        float sv[4];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int r = warp * 16 + kq + rr * 8;
+        for (int ps = 0; ps < 4; ++ps) {
+            const int r = warp * 16 + ps * 4 + kq;
+            float2 acc[GC];
 #pragma unroll
-            for (int h = 0; h < GC; ++h) s[rr][h] = 0.f;
+            for (int h = 0; h < GC; ++h) acc[h] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c8 = 0; c8 < DQ / 8; ++c8) {
-                const int dim = dq * DQ + c8 * 8;             // first of 8 dims
+                const int dim = dq * DQ + c8 * 8;
                 const int slab = dim >> 6, chunk = (dim & 63) >> 3;
                 const uint4 w = *reinterpret_cast<const uint4*>(ks + slab * C::SLAB + swz(r, chunk));
-                const float kf[8] = {bf16lo(w.x), bf16hi(w.x), bf16lo(w.y), bf16hi(w.y),
-                                     bf16lo(w.z), bf16hi(w.z), bf16lo(w.w), bf16hi(w.w)};
+                const float2 k2[4] = {make_float2(bf16lo(w.x), bf16hi(w.x)), make_float2(bf16lo(w.y), bf16hi(w.y)),
+                                      make_float2(bf16lo(w.z), bf16hi(w.z)), make_float2(bf16lo(w.w), bf16hi(w.w))};
 #pragma unroll
                 for (int h = 0; h < GC; ++h)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) s[rr][h] = fmaf(qv[h][c8 * 8 + i], kf[i], s[rr][h]);
+                    for (int i = 0; i < 4; ++i) acc[h] = __ffma2_rn(q2[h][c8 * 4 + i], k2[i], acc[h]);
             }
-        }
+            float v[GC];
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
+            for (int h = 0; h < GC; ++h) v[h] = acc[h].x + acc[h].y;
+            // reduce-scatter over the 8 dimension-group lanes (xor 4, 2, 1)
+            int n = GC;
 #pragma unroll
-            for (int h = 0; h < GC; ++h) {
-                s[rr][h] += __shfl_xor_sync(0xffffffffu, s[rr][h], 1);
-                s[rr][h] += __shfl_xor_sync(0xffffffffu, s[rr][h], 2);
+            for (int lv = 0; lv < 3; ++lv) {
+                const int mask = 4 >> lv;
+                if (n >= 2) {
+                    const bool up = (dq & mask) != 0;
+                    const int half = n / 2;
+#pragma unroll
+                    for (int i = 0; i < GC / 2; ++i) {
+                        if (i < half) {
+                            const float send = up ? v[i] : v[half + i];
+                            const float keep = up ? v[half + i] : v[i];
+                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+                        }
+                    }
+                    n = half;
+                } else {
+                    v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+                }
             }
-        // ---- logits (base 2), mask, running max per head
-        float mt[GC];
+            sv[ps] = v[0];
+        }
+        // ---- logits (base 2), mask, running max of this lane's head over the warp's 16 keys
+        float mt = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < GC; ++h) mt[h] = -INFINITY;
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int kj = t * TILE + warp * 16 + kq + rr * 8;
-#pragma unroll
-            for (int h = 0; h < GC; ++h) {
-                float x = s[rr][h];
-                if (SOFTCAP) x = p.softcap * LOG2E * tanhf(x / p.softcap);
-                if (ALIBI) x = fmaf(slope_l2[h], (float)kj, x);
-                if (kj >= p.Sk) x = -INFINITY;
-                s[rr][h] = x;
-                mt[h] = fmaxf(mt[h], x);
+        for (int ps = 0; ps < 4; ++ps) {
+            const int kj = t * TILE + warp * 16 + ps * 4 + kq;
+            float x = sv[ps];
+            if (SOFTCAP) {
+                // cap * tanh(y) with tanh(y) = 1 - 2 / (e^{2y} + 1), y = score / cap, times log2(e)
+                const float e = ex2_approx(x * (2.f * LOG2E / p.softcap));
+                x = p.softcap * LOG2E * (1.f - 2.f / (e + 1.f));
             }
+            if (ALIBI) x = fmaf(slope_l2, (float)kj, x);
+            if (kj >= p.Sk) x = -INFINITY;
+            sv[ps] = x;
+            mt = fmaxf(mt, x);
         }
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        const float m_new = fmaxf(m_h, mt);
+        const float alpha = (m_h == -INFINITY) ? 0.f : ex2_approx(m_h - m_new);
+        const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+        float psum = 0.f;
 #pragma unroll
-        for (int h = 0; h < GC; ++h) {
-            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 4));
-            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 8));
-            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], 16));
+        for (int ps = 0; ps < 4; ++ps) {
+            const float pv = ex2_approx(sv[ps] - m_ref);
+            psum += pv;
+            if (writer) p_s[warp][ps * 4 + kq][hsel] = make_float2(pv, pv);
         }
-        float pj[2][GC];
-#pragma unroll
-        for (int h = 0; h < GC; ++h) {
-            const float m_new = fmaxf(m[h], mt[h]);
-            const float alpha = (m[h] == -INFINITY) ? 0.f : ex2_approx(m[h] - m_new);
-            const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
-            pj[0][h] = ex2_approx(s[0][h] - m_ref);
-            pj[1][h] = ex2_approx(s[1][h] - m_ref);
-            if (m_new != -INFINITY) {
-                l[h] = l[h] * alpha + (pj[0][h] + pj[1][h]);
-#pragma unroll
-                for (int c = 0; c < DV; ++c) o[h][c] *= alpha;
-                m[h] = m_new;
-            }
+        if (m_new != -INFINITY) {
+            l_h = fmaf(l_h, alpha, psum);
+            m_h = m_new;
         }
-        if (dq == 0) {
-#pragma unroll
-            for (int h = 0; h < GC; ++h) {
-                p_s[warp][kq][h] = pj[0][h];
-                p_s[warp][kq + 8][h] = pj[1][h];
-            }
-        }
+        if (writer && kq == 0) a_s[warp][hsel] = (m_new != -INFINITY) ? make_float2(alpha, alpha) : make_float2(1.f, 1.f);
         __syncwarp();
-        // ---- P V over the warp's 16 keys; lane owns dims [lane*DV, lane*DV + DV)
+        // ---- rescale and P V over the warp's 16 keys; lane owns dims [lane*DV, lane*DV + DV)
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            const float2 a2 = a_s[warp][h];
+#pragma unroll
+            for (int c = 0; c < DV / 2; ++c) o2[h][c] = __fmul2_rn(o2[h][c], a2);
+        }
         {
             const int dim = lane * DV;
             const int slab = dim >> 6, chunk = (dim & 63) >> 3, within = (dim & 7) * 2;  // bytes
@@ -262,35 +282,21 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
             for (int j = 0; j < 16; ++j) {
                 const int r = warp * 16 + j;
                 const uint8_t* vp = vs + slab * C::SLAB + swz(r, chunk) + within;
-                float vf[DV];
+                float2 v2[DV / 2];
                 if (DV == 4) {
                     const uint2 w = *reinterpret_cast<const uint2*>(vp);
-                    vf[0] = bf16lo(w.x);
-                    vf[1] = bf16hi(w.x);
-                    vf[2] = bf16lo(w.y);
-                    vf[3] = bf16hi(w.y);
+                    v2[0] = make_float2(bf16lo(w.x), bf16hi(w.x));
+                    v2[DV / 2 - 1] = make_float2(bf16lo(w.y), bf16hi(w.y));
                 } else {
                     const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-                    vf[0] = bf16lo(w);
-                    vf[1] = bf16hi(w);
-                }
-                float pr[GC];
-#pragma unroll
-                for (int h = 0; h < GC; h += 4) {
-                    if (GC - h >= 4) {
-                        const float4 t4 = *reinterpret_cast<const float4*>(&p_s[warp][j][h]);
-                        pr[h] = t4.x;
-                        pr[h + 1] = t4.y;
-                        pr[h + 2] = t4.z;
-                        pr[h + 3] = t4.w;
-                    } else {
-                        for (int i = h; i < GC; ++i) pr[i] = p_s[warp][j][i];
-                    }
+                    v2[0] = make_float2(bf16lo(w), bf16hi(w));
                 }
 #pragma unroll
-                for (int h = 0; h < GC; ++h)
+                for (int h = 0; h < GC; ++h) {
+                    const float2 pp = p_s[warp][j][h];
 #pragma unroll
-                    for (int c = 0; c < DV; ++c) o[h][c] = fmaf(pr[h], vf[c], o[h][c]);
+                    for (int c = 0; c < DV / 2; ++c) o2[h][c] = __ffma2_rn(pp, v2[c], o2[h][c]);
+                }
             }
         }
         __syncwarp();
@@ -298,23 +304,17 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     }
 
     // ---- merge the four warps' states (fixed order), then write
-#pragma unroll
-    for (int h = 0; h < GC; ++h) {
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 4);
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
-        l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < GC; ++h) {
-            red_m[warp][h] = m[h];
-            red_l[warp][h] = l[h];
-        }
+    l_h += __shfl_xor_sync(0xffffffffu, l_h, 8);
+    l_h += __shfl_xor_sync(0xffffffffu, l_h, 16);
+    if (writer && kq == 0) {
+        red_m[warp][hsel] = m_h;
+        red_l[warp][hsel] = l_h;
     }
 #pragma unroll
     for (int h = 0; h < GC; ++h)
 #pragma unroll
-        for (int c = 0; c < DV; ++c) red_o[warp][h][lane * DV + c] = o[h][c];
+        for (int c = 0; c < DV / 2; ++c)
+            *reinterpret_cast<float2*>(&red_o[warp][h][lane * DV + 2 * c]) = o2[h][c];
     asm volatile("bar.sync 1, %0;" ::"n"(CONSUMERS * 32) : "memory");
     if (!ok || abort_flag) return;
 
