@@ -62,6 +62,14 @@ constexpr int EPI_REGS = 64;
 constexpr int CONTROL_REGS = 80;
 static_assert(2 * 128 * SOFTMAX_REGS + 128 * EPI_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS,
               "register split");
+// K/V tiles move through the shared-memory slots in the order the MMA thread
+// reads them: per item K_lo, then (V_u, K_{u+1}) for each tile u, V_hi last.
+// Each of these groups is one MMA step and has one full barrier (the TMA
+// transaction count of its one or two tiles) and one empty barrier (one
+// commit after the step's MMAs), so a step costs the MMA thread one wait and
+// one commit.  NG group barriers cycle; a slot is refilled only after the
+// group that last used it was released, at most NS groups back, so NG >= NS.
+constexpr int NG = 8;
 
 template <int D>
 struct Cfg {
@@ -180,7 +188,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
 struct Smem {
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], l_full[2];
-    uint64_t kv_full[8], kv_empty[8];
+    uint64_t grp_full[NG], grp_empty[NG];  // one per step group of K/V tiles
     uint64_t drain;
     float l_buf[2][2][BM];  // [item parity][slot][row]: softmax denominator l
     float m_buf[2][2][BM];  // running max (base 2) for lse
@@ -398,9 +406,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&sm.o_empty[x], BM);
             mbar_init(&sm.l_full[x], BM);
         }
-        for (int i = 0; i < C::NS; ++i) {
-            mbar_init(&sm.kv_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
+        for (int i = 0; i < NG; ++i) {
+            mbar_init(&sm.grp_full[i], 1);
+            mbar_init(&sm.grp_empty[i], 1);
         }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
@@ -433,7 +441,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_prefetch_desc(&tmK);
                 tma_prefetch_desc(&tmV);
             }
-            uint32_t kv_cnt = 0, q_cnt[2] = {0, 0};
+            uint32_t ld_cnt = 0, grp_cnt = 0, q_cnt[2] = {0, 0};
+            int slot_grp[C::NS];  // group that last filled each slot (-1: none)
+#pragma unroll
+            for (int i = 0; i < C::NS; ++i) slot_grp[i] = -1;
             bool ok = true;
             for (int k = 0;; ++k) {
                 const int item = item_of(k, cta, grid);
@@ -461,20 +472,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ulo = min(ulo, s[x].lo);
                             uhi = max(uhi, s[x].hi);
                         }
-                    for (int u = ulo; u <= uhi && ok; ++u) {
+                    // groups: (K_lo), then (V_u, K_{u+1}) for u < hi, then (V_hi)
+                    for (int u = ulo - 1; u <= uhi && ok; ++u) {
+                        const bool has_v = u >= ulo, has_k = u < uhi;
+                        const int nl = (has_v ? 1 : 0) + (has_k ? 1 : 0);
+                        // both slots must have been released by the groups that last used them
 #pragma unroll
-                        for (int kv = 0; kv < 2; ++kv) {
-                            const int st = kv_cnt % C::NS;
-                            ok = mbar_wait(&sm.kv_empty[st], ((kv_cnt / C::NS) & 1) ^ 1, wc, ST_PREFILL_PRODUCER);
-                            if (!ok) break;
-                            mbar_arrive_expect_tx(&sm.kv_full[st], C::KV_BYTES);
+                        for (int i = 0; i < 2; ++i) {
+                            if (i >= nl) break;
+                            const int g_prev = slot_grp[(ld_cnt + i) % C::NS];
+                            if (g_prev >= 0)
+                                ok = ok && mbar_wait(&sm.grp_empty[g_prev % NG], (g_prev / NG) & 1, wc,
+                                                     ST_PREFILL_PRODUCER);
+                        }
+                        if (!ok) break;
+                        uint64_t* fb = &sm.grp_full[grp_cnt % NG];
+                        mbar_arrive_expect_tx(fb, nl * C::KV_BYTES);
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            if (i >= nl) break;
+                            const bool is_v = has_v && i == 0;
+                            const int st = (ld_cnt + i) % C::NS;
                             uint8_t* dst = sKV + st * C::KV_BYTES;
 #pragma unroll
                             for (int hf = 0; hf < C::HALVES; ++hf)
-                                tma_load_3d(dst + hf * C::KV_SLAB, kv ? &tmV : &tmK, &sm.kv_full[st], hf * 64,
-                                            u * BN, s[0].b * p.Hkv + hkv);
-                            ++kv_cnt;
+                                tma_load_3d(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64,
+                                            (is_v ? u : u + 1) * BN, s[0].b * p.Hkv + hkv);
+                            slot_grp[st] = (int)grp_cnt;
                         }
+                        ld_cnt += nl;
+                        ++grp_cnt;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -482,9 +509,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (!ok && lane == 0) {
                 // Let the copies already issued land before the CTA leaves.
-                const uint32_t n = kv_cnt < (uint32_t)C::NS ? kv_cnt : (uint32_t)C::NS;
-                for (uint32_t i = kv_cnt - n; i < kv_cnt; ++i)
-                    mbar_drain(&sm.kv_full[i % C::NS], (i / C::NS) & 1, 100000000ull);
+                const uint32_t n = grp_cnt < (uint32_t)NG ? grp_cnt : (uint32_t)NG;
+                for (uint32_t i = grp_cnt - n; i < grp_cnt; ++i)
+                    mbar_drain(&sm.grp_full[i % NG], (i / NG) & 1, 100000000ull);
 #pragma unroll
                 for (int x = 0; x < 2; ++x)
                     if (q_cnt[x]) mbar_drain(&sm.q_full[x], (q_cnt[x] - 1) & 1, 100000000ull);
@@ -493,7 +520,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // -------------------------------------------------------- MMA issuer
             constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
-            uint32_t kv_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
+            uint32_t ld_cnt = 0, grp_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
             bool ok = true;
             const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
             const uint32_t sKVa = smem_u32(sKV);
@@ -534,29 +561,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         return true;
                     };
                     if (ulo <= uhi) {
-                        // prologue: K of the first tile
-                        uint32_t kst = kv_cnt % C::NS;
-                        ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
-                        ++kv_cnt;
+                        // prologue step: group (K_lo)
+                        uint32_t gb = grp_cnt % NG;
+                        ok = mbar_wait(&sm.grp_full[gb], (grp_cnt / NG) & 1, wc, ST_PREFILL_MMA);
+                        ++grp_cnt;
+                        uint32_t kst = ld_cnt % C::NS;
+                        ld_cnt += 1;
                         if (ok) tc_fence_after();
 #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x)
                             if (in_range(s[x], ulo)) ok = issue_s(x, kst, ulo);
-                        if (ok) umma_commit(&sm.kv_empty[kst]);
+                        if (ok) umma_commit(&sm.grp_empty[gb]);
                         for (int u = ulo; u <= uhi && ok; ++u) {
-                            // Wait for V_u and K_{u+1} up front, so that each slot's
-                            // P V and next Q K^T go to the tensor pipe as one run.
-                            const uint32_t vst = kv_cnt % C::NS;
-                            ok = mbar_wait(&sm.kv_full[vst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
-                            ++kv_cnt;
-                            if (!ok) break;
+                            // step u: group (V_u, K_{u+1}); each slot's P V and next
+                            // Q K^T then go to the tensor pipe as one run
                             const bool has_next = u < uhi;
-                            if (has_next) {
-                                kst = kv_cnt % C::NS;
-                                ok = mbar_wait(&sm.kv_full[kst], (kv_cnt / C::NS) & 1, wc, ST_PREFILL_MMA);
-                                ++kv_cnt;
-                                if (!ok) break;
-                            }
+                            gb = grp_cnt % NG;
+                            ok = mbar_wait(&sm.grp_full[gb], (grp_cnt / NG) & 1, wc, ST_PREFILL_MMA);
+                            ++grp_cnt;
+                            if (!ok) break;
+                            const uint32_t vst = ld_cnt % C::NS;
+                            kst = (ld_cnt + 1) % C::NS;
+                            ld_cnt += has_next ? 2 : 1;
                             tc_fence_after();
 #pragma unroll
                             for (int x = 0; x < 2 && ok; ++x) {
@@ -581,8 +607,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 if (has_next && in_range(s[x], u + 1)) ok = issue_s(x, kst, u + 1);
                             }
                             if (!ok) break;
-                            umma_commit(&sm.kv_empty[vst]);
-                            if (has_next) umma_commit(&sm.kv_empty[kst]);
+                            umma_commit(&sm.grp_empty[gb]);
                         }
                     }
                 }
