@@ -518,6 +518,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         } else if (warp == WARP_MMA) {
             // -------------------------------------------------------- MMA issuer
+            // The whole warp runs the loop and one elected lane issues each MMA and
+            // commit (warp-collective forms keep the operands in uniform registers;
+            // a single thread can issue a tcgen05.mma only every ~40 cycles while an
+            // M=128 N=128 K=16 MMA takes 64).  Waits are warp votes, so the warp
+            // stays converged.
+            auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, ST_PREFILL_MMA));
+            };
             constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
             uint32_t ld_cnt = 0, grp_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
@@ -529,7 +537,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (item >= p.n_items) break;
                 Slot s[2];
                 decode_item(p, item, s);
-                if (lane == 0) {
+                {
                     int ulo = 0x7fffffff, uhi = -1;
 #pragma unroll
                     for (int x = 0; x < 2; ++x)
@@ -542,7 +550,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // at once, so the next item's Q load overlaps this item's tail.
                     auto issue_s = [&](int x, uint32_t kst, int ut) -> bool {
                         if (!q_ready[x]) {
-                            if (!mbar_wait(&sm.q_full[x], q_cnt[x] & 1, wc, ST_PREFILL_MMA)) return false;
+                            if (!wwait(&sm.q_full[x], q_cnt[x] & 1)) return false;
                             ++q_cnt[x];
                             q_ready[x] = true;
                             tc_fence_after();
@@ -554,43 +562,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = ((kk >> 2) * C::Q_SLAB + (kk & 3) * 32) >> 4;
                             const uint32_t koff = ((kk >> 2) * C::KV_SLAB + (kk & 3) * 32) >> 4;
-                            umma_ss_lo(dS, qlo + off, klo + koff, IDESC_S, kk > 0);
+                            umma_ss_lo_elect(dS, qlo + off, klo + koff, IDESC_S, kk > 0);
                         }
-                        umma_commit(&sm.s_full[x]);
-                        if (ut == s[x].hi) umma_commit(&sm.q_empty[x]);
+                        umma_commit_elect(&sm.s_full[x]);
+                        if (ut == s[x].hi) umma_commit_elect(&sm.q_empty[x]);
                         return true;
                     };
                     if (ulo <= uhi) {
                         // prologue step: group (K_lo)
                         uint32_t gb = grp_cnt % NG;
-                        ok = mbar_wait(&sm.grp_full[gb], (grp_cnt / NG) & 1, wc, ST_PREFILL_MMA);
+                        ok = wwait(&sm.grp_full[gb], (grp_cnt / NG) & 1);
                         ++grp_cnt;
                         uint32_t kst = ld_cnt % C::NS;
                         ld_cnt += 1;
-                        if (ok) tc_fence_after();
 #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x)
                             if (in_range(s[x], ulo)) ok = issue_s(x, kst, ulo);
-                        if (ok) umma_commit(&sm.grp_empty[gb]);
+                        if (ok) umma_commit_elect(&sm.grp_empty[gb]);
                         for (int u = ulo; u <= uhi && ok; ++u) {
                             // step u: group (V_u, K_{u+1}); each slot's P V and next
                             // Q K^T then go to the tensor pipe as one run
                             const bool has_next = u < uhi;
                             gb = grp_cnt % NG;
-                            ok = mbar_wait(&sm.grp_full[gb], (grp_cnt / NG) & 1, wc, ST_PREFILL_MMA);
+                            ok = wwait(&sm.grp_full[gb], (grp_cnt / NG) & 1);
                             ++grp_cnt;
                             if (!ok) break;
                             const uint32_t vst = ld_cnt % C::NS;
                             kst = (ld_cnt + 1) % C::NS;
                             ld_cnt += has_next ? 2 : 1;
-                            tc_fence_after();
 #pragma unroll
                             for (int x = 0; x < 2 && ok; ++x) {
                                 if (in_range(s[x], u)) {
-                                    ok = mbar_wait(&sm.p_full[x], p_cnt[x] & 1, wc, ST_PREFILL_MMA);
+                                    ok = wwait(&sm.p_full[x], p_cnt[x] & 1);
                                     ++p_cnt[x];
                                     if (ok && u == s[x].lo) {
-                                        ok = mbar_wait(&sm.o_empty[x], (o_cnt[x] & 1) ^ 1, wc, ST_PREFILL_MMA);
+                                        ok = wwait(&sm.o_empty[x], (o_cnt[x] & 1) ^ 1);
                                         ++o_cnt[x];
                                     }
                                     if (!ok) break;
@@ -600,18 +606,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     const uint32_t acc0 = (u > s[x].lo) ? 1u : 0u;
 #pragma unroll
                                     for (int kk = 0; kk < BN / 16; ++kk)
-                                        umma_ts_lo(dO, aP + 8u * kk, vlo + ((kk * 16 * 128) >> 4), IDESC_O,
-                                                   kk > 0 ? 1u : acc0);
-                                    if (u == s[x].hi) umma_commit(&sm.o_full[x]);
+                                        umma_ts_lo_elect(dO, aP + 8u * kk, vlo + ((kk * 16 * 128) >> 4), IDESC_O,
+                                                         kk > 0 ? 1u : acc0);
+                                    if (u == s[x].hi) umma_commit_elect(&sm.o_full[x]);
                                 }
                                 if (has_next && in_range(s[x], u + 1)) ok = issue_s(x, kst, u + 1);
                             }
                             if (!ok) break;
-                            umma_commit(&sm.grp_empty[gb]);
+                            umma_commit_elect(&sm.grp_empty[gb]);
                         }
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
             }
             if (lane == 0) {
