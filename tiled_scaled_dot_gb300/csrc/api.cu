@@ -192,12 +192,13 @@ int attn_fwd_ex(const gbattn_fwd_params* a) {
     if (a->dtype == GBATTN_F32) {
         e = launch_prefill_f32(f, st);
     } else {
-        CUtensorMap tq, tk, tv;
+        CUtensorMap tq, tk, tv, to;
         if (!cached_map(&tq, a->q, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128) ||
             !cached_map(&tk, a->k, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128) ||
-            !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128))
+            !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128) ||
+            !cached_map(&to, a->out, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128))
             return GBATTN_ERR_CUDA;
-        e = launch_prefill_bf16(f, tq, tk, tv, st);
+        e = launch_prefill_bf16(f, tq, tk, tv, to, st);
     }
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }

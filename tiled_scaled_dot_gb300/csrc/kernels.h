@@ -64,7 +64,7 @@ bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint6
 
 // Kernel launchers.  Each returns the launch's cudaError_t.
 cudaError_t launch_prefill_bf16(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, cudaStream_t stream);
+                                const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream);
 cudaError_t launch_prefill_f32(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream);

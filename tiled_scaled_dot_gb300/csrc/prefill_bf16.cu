@@ -79,7 +79,8 @@ struct Cfg {
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int KV_SLAB = BN * 128;
     static constexpr int NS = (D == 128) ? 4 : 6;     // K/V ring stages
-    static constexpr int SMEM_BYTES = 2 * Q_BYTES + NS * KV_BYTES + 1024;  // + alignment slack
+    static constexpr int STAGE_O = BM * 128;          // output staging: 128 rows x 64 columns bf16
+    static constexpr int SMEM_BYTES = 2 * Q_BYTES + NS * KV_BYTES + STAGE_O + 1024;  // + alignment slack
     static constexpr int O_COL = 256;
 };
 
@@ -321,11 +322,18 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
 // ---------------------------------------------------------------------------- epilogue role
 template <int D>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_t tmem, const WaitCtl& wc,
-                                              int warp) {
+                                              int warp, uint8_t* stage, const CUtensorMap* tmO) {
+    // Output rows go through a 128-row x 64-column bf16 staging tile in shared
+    // memory (128-byte swizzle: thread r writes row r without bank conflicts)
+    // and leave by TMA tensor stores, which write whole lines and clip the rows
+    // past Sq.  One elected thread issues the stores and waits for their reads
+    // of the staging tile before it is refilled.
     using C = Cfg<D>;
     const int r = threadIdx.x & (BM - 1);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int grid = gridDim.x, cta = blockIdx.x;
+    const bool issuer = (threadIdx.x & (BM - 1)) == 0;
+    uint8_t* srow = stage + r * 128;
     uint32_t cnt[2] = {0, 0};
     for (int k = 0;; ++k) {
         const int item = item_of(k, cta, grid);
@@ -360,30 +368,48 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
             const uint32_t tO = tmem + lane_off + C::O_COL + D * x;
 #pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                float ov[32];
-                tmem_ld32(tO + c, ov);
-                if (live) {
-                    uint32_t w[16];
+            for (int hf = 0; hf < C::HALVES; ++hf) {
+                // the staging tile is free once the previous store has read it
+                if (issuer) bulk_wait_group_read0();
+                asm volatile("bar.sync 1, %0;" ::"n"(BM) : "memory");
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(ov[2 * i] * inv_l, ov[2 * i + 1] * inv_l);
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * D + c);
+                for (int c32 = 0; c32 < 2; ++c32) {
+                    float ov[32];
+                    tmem_ld32(tO + hf * 64 + c32 * 32, ov);
+                    if (hf == C::HALVES - 1 && c32 == 1) {
+                        // all of O_x has been read: the next item may overwrite it
+                        tc_fence_before();
+                        mbar_arrive(&sm.o_empty[x]);
+                    }
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = c32 * 4 + i;  // 16-byte chunk of the 128-byte staging row
+                        uint4 w;
+                        w.x = pack_bf16x2(ov[8 * i + 0] * inv_l, ov[8 * i + 1] * inv_l);
+                        w.y = pack_bf16x2(ov[8 * i + 2] * inv_l, ov[8 * i + 3] * inv_l);
+                        w.z = pack_bf16x2(ov[8 * i + 4] * inv_l, ov[8 * i + 5] * inv_l);
+                        w.w = pack_bf16x2(ov[8 * i + 6] * inv_l, ov[8 * i + 7] * inv_l);
+                        *reinterpret_cast<uint4*>(srow + ((c ^ (r & 7)) << 4)) = w;
+                    }
+                }
+                fence_proxy_async_smem();
+                asm volatile("bar.sync 1, %0;" ::"n"(BM) : "memory");
+                if (issuer) {
+                    tma_store_3d(tmO, stage, hf * 64, sl.t * BM, sl.b * p.Hq + sl.h);
+                    bulk_commit_group();
                 }
             }
             if (live && p.lse) p.lse[row] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
-            tc_fence_before();
-            mbar_arrive(&sm.o_empty[x]);
         }
     }
+    if (issuer) bulk_wait_group0();
 }
 
 template <int D, bool SOFTCAP, bool ALIBI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const Params p) {
+                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                        const Params p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t dyn_smem[];
     __shared__ Smem sm;
@@ -391,6 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ[2] = {base, base + C::Q_BYTES};
     uint8_t* sKV = base + 2 * C::Q_BYTES;
+    uint8_t* sStage = sKV + C::NS * C::KV_BYTES;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -431,7 +458,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         softmax_role<D, SOFTCAP, ALIBI>(p, sm, tmem, wc, warp);
     } else if (warp < 12) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
-        epilogue_role<D>(p, sm, tmem, wc, warp);
+        epilogue_role<D>(p, sm, tmem, wc, warp, sStage, &tmO);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CONTROL_REGS));
         if (warp == WARP_PRODUCER) {
@@ -637,7 +664,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <int D, bool SOFTCAP, bool ALIBI>
 cudaError_t launch_variant(const Params& prm, int grid, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, cudaStream_t stream) {
+                           const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
     auto kern = prefill_bf16_kernel<D, SOFTCAP, ALIBI>;
     const int smem = Cfg<D>::SMEM_BYTES;
     cudaFuncAttributes fa{};
@@ -648,14 +675,14 @@ cudaError_t launch_variant(const Params& prm, int grid, const CUtensorMap& tq, c
     if (fa.numRegs < LAUNCH_REGS) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tk, tv, prm);
+    kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tk, tv, to, prm);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, cudaStream_t stream) {
+                                const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
     Params p{};
     p.out = static_cast<__nv_bfloat16*>(f.out);
     p.lse = f.lse;
@@ -684,15 +711,15 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
     const int grid = p.n_items < f.num_sms ? p.n_items : f.num_sms;
     const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
     if (f.D == 128) {
-        if (cap) return ali ? launch_variant<128, true, true>(p, grid, tq, tk, tv, stream)
-                            : launch_variant<128, true, false>(p, grid, tq, tk, tv, stream);
-        return ali ? launch_variant<128, false, true>(p, grid, tq, tk, tv, stream)
-                   : launch_variant<128, false, false>(p, grid, tq, tk, tv, stream);
+        if (cap) return ali ? launch_variant<128, true, true>(p, grid, tq, tk, tv, to, stream)
+                            : launch_variant<128, true, false>(p, grid, tq, tk, tv, to, stream);
+        return ali ? launch_variant<128, false, true>(p, grid, tq, tk, tv, to, stream)
+                   : launch_variant<128, false, false>(p, grid, tq, tk, tv, to, stream);
     }
-    if (cap) return ali ? launch_variant<64, true, true>(p, grid, tq, tk, tv, stream)
-                        : launch_variant<64, true, false>(p, grid, tq, tk, tv, stream);
-    return ali ? launch_variant<64, false, true>(p, grid, tq, tk, tv, stream)
-               : launch_variant<64, false, false>(p, grid, tq, tk, tv, stream);
+    if (cap) return ali ? launch_variant<64, true, true>(p, grid, tq, tk, tv, to, stream)
+                        : launch_variant<64, true, false>(p, grid, tq, tk, tv, to, stream);
+    return ali ? launch_variant<64, false, true>(p, grid, tq, tk, tv, to, stream)
+               : launch_variant<64, false, false>(p, grid, tq, tk, tv, to, stream);
 }
 
 }  // namespace gbattn
