@@ -94,7 +94,7 @@ struct Params {
     int B, Hq, Hkv, Sq, Sk, G;
     int causal, wl, wr;
     float scale_log2;  // softmax_scale * log2(e)
-    float cap_e2;      // 2 * softmax_scale / softcap * log2(e): 2^(s cap_e2) = e^(2 scale s / c)
+    float cap_in;      // softmax_scale / softcap
     float cap_out;     // softcap * log2(e)
     int n_qt;          // query tiles per head
     int pair_heads;    // 1: slots are heads (2p, 2p+1) at one row tile; 0: row tiles (2t, 2t+1) of one head
@@ -180,9 +180,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
-__device__ __forceinline__ float rcp_approx(float x) {
+__device__ __forceinline__ float tanh_approx(float x) {
     float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -233,18 +233,20 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
             tmem_ld64(tS + 64, *reinterpret_cast<float(*)[64]>(&sv[64]));
             const int k0 = u * BN;
             if (SOFTCAP || ALIBI) {
-                // base-2 logits: cap * tanh(scale s / cap) [+ slope (kj - qi)], times log2(e);
-                // tanh(y) = 1 - 2 / (e^{2y} + 1)
+                // base-2 logits: cap * tanh(scale s / cap) [+ slope (kj - qi)], times log2(e).
+                // tanh is the hardware approximation (relative error about 2^-11,
+                // far below the bf16 rounding of P); the ALiBi bias of key k0 + j is
+                // base + slope * j with one conversion per tile.
+                const float abase = ALIBI ? slope_l2 * (float)(k0 - qi) : 0.f;
 #pragma unroll
                 for (int j = 0; j < BN; ++j) {
                     float t;
                     if (SOFTCAP) {
-                        const float e = ex2_approx(sv[j] * p.cap_e2);
-                        t = fmaf(-2.f * p.cap_out, rcp_approx(e + 1.f), p.cap_out);
+                        t = p.cap_out * tanh_approx(sv[j] * p.cap_in);
                     } else {
                         t = sv[j] * p.scale_log2;
                     }
-                    if (ALIBI) t = fmaf(slope_l2, (float)(k0 + j - qi), t);
+                    if (ALIBI) t += fmaf(slope_l2, (float)j, abase);
                     sv[j] = t;
                 }
             }
@@ -700,7 +702,7 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
     p.wl = f.wl;
     p.wr = f.wr;
     p.scale_log2 = f.scale * LOG2E;
-    p.cap_e2 = f.softcap > 0.f ? 2.f * f.scale / f.softcap * LOG2E : 0.f;
+    p.cap_in = f.softcap > 0.f ? f.scale / f.softcap : 0.f;
     p.cap_out = f.softcap * LOG2E;
     p.n_qt = (f.Sq + BM - 1) / BM;
     p.pair_heads = (p.G % 2 == 0) ? 1 : 0;
