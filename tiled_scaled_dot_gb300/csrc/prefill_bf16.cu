@@ -35,8 +35,8 @@
 //
 // Causal and window tile skipping ("gfx942 unified attention", section 4): a
 // slot visits only the key tiles that intersect the union of its rows'
-// admissible ranges; element masks are applied only on tiles that cut a row's
-// range.  Lazy rescaling: O and l are rescaled only when the running max grows
+// admissible ranges, last tile first; element masks are applied only on tiles
+// that cut a row's range.  Lazy rescaling: O and l are rescaled only when the running max grows
 // by more than 8 (base-2 units); otherwise the stale max stays the reference,
 // which keeps every p <= 2^8 and leaves o / l exact.
 #include <cuda_bf16.h>
@@ -223,7 +223,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
         float slope_l2 = 0.f;
         if (ALIBI) slope_l2 = __ldg(p.slopes + sl.h) * LOG2E;
         float m_used = -INFINITY, l = 0.f;
-        for (int u = sl.lo; u <= sl.hi; ++u) {
+        for (int u = sl.hi; u >= sl.lo; --u) {
             const bool ok = mbar_wait(&sm.s_full[x], s_cnt & 1, wc, ST_PREFILL_SOFTMAX);
             ++s_cnt;
             if (!__all_sync(0xffffffffu, ok)) return;
@@ -501,9 +501,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ulo = min(ulo, s[x].lo);
                             uhi = max(uhi, s[x].hi);
                         }
-                    // groups: (K_lo), then (V_u, K_{u+1}) for u < hi, then (V_hi)
-                    for (int u = ulo - 1; u <= uhi && ok; ++u) {
-                        const bool has_v = u >= ulo, has_k = u < uhi;
+                    // Key tiles are visited from the last one back (the order of the
+                    // recurrence is free; with ALiBi or causal masks the largest scores
+                    // sit near the diagonal, so the running max settles at once).
+                    // groups: (K_hi), then (V_u, K_{u-1}) for u > lo, then (V_lo)
+                    const int nt = uhi - ulo + 1;
+                    for (int i = -1; i < nt && ok; ++i) {
+                        const int u = uhi - i;  // V tile of this group; its K tile is u - 1
+                        const bool has_v = i >= 0, has_k = i < nt - 1;
                         const int nl = (has_v ? 1 : 0) + (has_k ? 1 : 0);
                         // both slots must have been released by the groups that last used them
 #pragma unroll
@@ -526,7 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                             for (int hf = 0; hf < C::HALVES; ++hf)
                                 tma_load_3d(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64,
-                                            (is_v ? u : u + 1) * BN, s[0].b * p.Hkv + hkv);
+                                            (is_v ? u : u - 1) * BN, s[0].b * p.Hkv + hkv);
                             slot_grp[st] = (int)grp_cnt;
                         }
                         ld_cnt += nl;
@@ -594,11 +599,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             umma_ss_lo_elect(dS, qlo + off, klo + koff, IDESC_S, kk > 0);
                         }
                         umma_commit_elect(&sm.s_full[x]);
-                        if (ut == s[x].hi) umma_commit_elect(&sm.q_empty[x]);
+                        if (ut == s[x].lo) umma_commit_elect(&sm.q_empty[x]);
                         return true;
                     };
                     if (ulo <= uhi) {
-                        // prologue step: group (K_lo)
+                        // prologue step: group (K_hi)
                         uint32_t gb = grp_cnt % NG;
                         ok = wwait(&sm.grp_full[gb], (grp_cnt / NG) & 1);
                         ++grp_cnt;
@@ -606,12 +611,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ld_cnt += 1;
 #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x)
-                            if (in_range(s[x], ulo)) ok = issue_s(x, kst, ulo);
+                            if (in_range(s[x], uhi)) ok = issue_s(x, kst, uhi);
                         if (ok) umma_commit_elect(&sm.grp_empty[gb]);
-                        for (int u = ulo; u <= uhi && ok; ++u) {
-                            // step u: group (V_u, K_{u+1}); each slot's P V and next
+                        for (int u = uhi; u >= ulo && ok; --u) {
+                            // step u: group (V_u, K_{u-1}); each slot's P V and next
                             // Q K^T then go to the tensor pipe as one run
-                            const bool has_next = u < uhi;
+                            const bool has_next = u > ulo;
                             gb = grp_cnt % NG;
                             ok = wwait(&sm.grp_full[gb], (grp_cnt / NG) & 1);
                             ++grp_cnt;
@@ -624,7 +629,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 if (in_range(s[x], u)) {
                                     ok = wwait(&sm.p_full[x], p_cnt[x] & 1);
                                     ++p_cnt[x];
-                                    if (ok && u == s[x].lo) {
+                                    if (ok && u == s[x].hi) {
                                         ok = wwait(&sm.o_empty[x], (o_cnt[x] & 1) ^ 1);
                                         ++o_cnt[x];
                                     }
@@ -632,14 +637,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     tc_fence_after();
                                     const uint32_t vlo = sdesc_lo(sKVa + vst * C::KV_BYTES, C::KV_SLAB);
                                     const uint32_t dO = tmem + C::O_COL + D * x, aP = tmem + 128u * x;
-                                    const uint32_t acc0 = (u > s[x].lo) ? 1u : 0u;
+                                    const uint32_t acc0 = (u < s[x].hi) ? 1u : 0u;
 #pragma unroll
                                     for (int kk = 0; kk < BN / 16; ++kk)
                                         umma_ts_lo_elect(dO, aP + 8u * kk, vlo + ((kk * 16 * 128) >> 4), IDESC_O,
                                                          kk > 0 ? 1u : acc0);
-                                    if (u == s[x].hi) umma_commit_elect(&sm.o_full[x]);
+                                    if (u == s[x].lo) umma_commit_elect(&sm.o_full[x]);
                                 }
-                                if (has_next && in_range(s[x], u + 1)) ok = issue_s(x, kst, u + 1);
+                                if (has_next && in_range(s[x], u - 1)) ok = issue_s(x, kst, u - 1);
                             }
                             if (!ok) break;
                             umma_commit_elect(&sm.grp_empty[gb]);
