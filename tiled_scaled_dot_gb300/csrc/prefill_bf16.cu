@@ -57,11 +57,6 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // base-2 units
 constexpr int LAUNCH_REGS = 128;          // 65536 / 512
-constexpr int SOFTMAX_REGS = 184;
-constexpr int EPI_REGS = 64;
-constexpr int CONTROL_REGS = 80;
-static_assert(2 * 128 * SOFTMAX_REGS + 128 * EPI_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS,
-              "register split");
 // K/V tiles move through the shared-memory slots in the order the MMA thread
 // reads them: per item K_lo, then (V_u, K_{u+1}) for each tile u, V_hi last.
 // Each of these groups is one MMA step and has one full barrier (the TMA
@@ -82,6 +77,14 @@ struct Cfg {
     static constexpr int STAGE_O = BM * 128;          // output staging: 128 rows x 64 columns bf16
     static constexpr int SMEM_BYTES = 2 * Q_BYTES + NS * KV_BYTES + STAGE_O + 1024;  // + alignment slack
     static constexpr int O_COL = 256;
+    // setmaxnreg budgets per warpgroup (multiples of 8); this split leaves ptxas
+    // spilling at most a few bytes in any variant, the 184/64/80 split spilled
+    // the epilogue and control loops
+    static constexpr int SOFTMAX_REGS = 176;
+    static constexpr int EPI_REGS = 72;
+    static constexpr int CONTROL_REGS = 88;
+    static_assert(2 * 128 * SOFTMAX_REGS + 128 * EPI_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS,
+                  "register split");
 };
 
 struct Params {
@@ -456,13 +459,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // Each warpgroup executes one setmaxnreg, at one program point, before its roles split.
     if (warp < 8) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(SOFTMAX_REGS));
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::SOFTMAX_REGS));
         softmax_role<D, SOFTCAP, ALIBI>(p, sm, tmem, wc, warp);
     } else if (warp < 12) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(EPI_REGS));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::EPI_REGS));
         epilogue_role<D>(p, sm, tmem, wc, warp, sStage, &tmO);
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CONTROL_REGS));
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::CONTROL_REGS));
         if (warp == WARP_PRODUCER) {
             // -------------------------------------------------------- TMA producer
             if (lane == 0) {
