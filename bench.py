@@ -3,9 +3,10 @@
 
 A step is one pass of the hot path over one batch of synthetic input:
   * prefill (the headline): attn_fwd on bf16 causal prefill B=4, Hq=32,
-    Hkv=8, S=2048, D=128 (rows a1-a8 of the path), inputs resident in HBM;
+    Hkv=8, S=2048, D=128 (tile loads, Q K^T, masks, online softmax, P V,
+    normalisation and store, all in one kernel launch), inputs resident in HBM;
   * decode (reported beside it): attn_decode on bf16 B=64, Hq=32, Hkv=8,
-    Sk=8192, D=128 (rows a9-a10).
+    Sk=8192, D=128 (split-KV partials and the log-sum-exp combine).
 value = causal-adjusted attention TFLOP/s (4 D flops per admissible
 (query, key) pair) over all ranks.  The decode object reports HBM GB/s of its
 algorithmic bytes (Q + K + V + O).
@@ -150,6 +151,34 @@ def max_over_ranks(x: float, ws: int) -> float:
     return float(t.item())
 
 
+# ----------------------------------------------------------------------------- ncu traffic
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel, from one ncu capture, keyed by a fingerprint of the
+# kernel's source files: a changed kernel reports null until it is captured
+# again.  The captures and their commands are summarised under profiles/.
+KERNEL_SOURCES = {
+    "prefill": ("prefill_bf16.cu", "ptx.cuh", "kernels.h"),
+    "decode": ("decode_bf16.cu", "ptx.cuh", "kernels.h"),
+}
+NCU_TRAFFIC = {
+    # (kernel, workload, source fingerprint): bytes per launch
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "b3c329451ce86a4e"): 129104128,
+}
+
+
+def kernel_fingerprint(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "tiled_scaled_dot_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kind, workload):
+    return NCU_TRAFFIC.get((kind, workload, kernel_fingerprint(kind)))
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def prefill_call(g, w, x, out):
     return g.attn_fwd(x["q"], x["k"], x["v"], x["alibi_slopes"], softmax_scale=w.scale, causal=w.causal,
@@ -210,7 +239,7 @@ def bench_prefill(g, w, args, ws, dev, pk):
     res = dict(ms_per_step=per_launch_ms, tflops_per_gpu=tflops, flops=flops, dense_flops=w.dense_flops(),
                rotation=n_copies, in_bytes=in_bytes)
     res["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
-                       "frac": round(tflops / pk["bf16"], 4), "traffic": None,
+                       "frac": round(tflops / pk["bf16"], 4), "traffic": ncu_traffic("prefill", w.name),
                        "peak_source": f"bf16_tflops ({pk['source']}, burst: the kernel is timed alone)"}
     if not args.no_e2e:
         res["e2e"] = e2e_prefill(g, w, base, args, ws, stream, flops)
@@ -267,9 +296,10 @@ def bench_decode(g, args, ws, dev, pk):
     splits = ws_bytes // (w.B * w.Hq * (w.D + 1) * 4) if ws_bytes else 1
     res = {"workload": DECODE, "metric": "decode HBM GB/s (Q+K+V+O bytes)", "value": round(gbs * ws, 1),
            "unit": "GB/s", "ms_per_step": round(per, 4), "bytes_per_step": nbytes,
-           "launches_per_step": 2 if ws_bytes else 1, "splits": int(splits),
+           "launches_per_step": 2 if ws_bytes else 1, "gpu_launches": args.steps * (2 if ws_bytes else 1),
+           "splits": int(splits),
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                        "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                        "frac": round(gbs / pk["hbm"], 4), "traffic": ncu_traffic("decode", w.name),
                         "peak_source": f"hbm_gbs ({pk['source']})", "frac_of_8tbs_nominal": round(gbs / 8000.0, 4)}}
     if not args.no_e2e:
         qh = x["q"].cpu().pin_memory()
@@ -320,13 +350,17 @@ def oracle_kwargs(w, x_cpu):
 
 def oracle_rows(w, x_cpu, seconds, seed=11):
     """A seeded row sample of the workload that takes the oracle about
-    `seconds`; returns (rows, seconds taken)."""
+    `seconds` (every row when the whole workload takes less); returns
+    (rows, seconds taken)."""
     import oracle
     import synth
     total_rows = w.B * w.Hq * w.Sq
     n = 64
     while True:
-        rows = torch.unique(synth.randint(n, total_rows, seed, 12))
+        if n >= total_rows:
+            rows = torch.arange(total_rows, dtype=torch.int64)
+        else:
+            rows = torch.unique(synth.randint(n, total_rows, seed, 12))
         t0 = time.time()
         oracle.attn(x_cpu["q"], x_cpu["k"], x_cpu["v"], rows=rows, **oracle_kwargs(w, x_cpu))
         dt = time.time() - t0
@@ -341,8 +375,12 @@ def oracle_sample(w, x_cpu, seconds):
     rows, dt = oracle_rows(w, x_cpu, seconds)
     flops = 4.0 * w.D * admissible_pairs(w, rows, x_cpu["row_kv_bounds"])
     total = w.B * w.Hq * w.Sq
-    return flops / dt / 1e12, f"{rows.numel()} seeded random query rows of {total} ({dt:.1f} s)", \
-        oracle.max_threads()
+    return flops / dt / 1e12, f"{sample_text(rows, total)} ({dt:.1f} s)", oracle.max_threads()
+
+
+def sample_text(rows, total):
+    return f"all {total} query rows" if rows.numel() == total else \
+        f"{rows.numel()} seeded random query rows of {total}"
 
 
 # ----------------------------------------------------------------------------- main
@@ -401,7 +439,6 @@ def main():
         line["e2e"] = pre["e2e"]
     if dec is not None:
         line["decode"] = dec
-        line["gpu_launches"] += args.steps * dec["launches_per_step"]
     if rank == 0 and not args.no_cpu_baseline:
         x_cpu = make_inputs(w, "cpu")
         tf, sample, threads = oracle_sample(w, x_cpu, args.cpu_seconds)
@@ -440,7 +477,7 @@ def main_reference(args, ws, rank, w):
                        "causal": w.causal},
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.max_threads(),
                              "kind": "oracle",
-                             "sample": f"{rows.numel()} seeded random query rows of {w.B * w.Hq * w.Sq} per step"},
+                             "sample": f"{sample_text(rows, w.B * w.Hq * w.Sq)} per step"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

@@ -232,8 +232,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
             if (!__all_sync(0xffffffffu, ok)) return;
             tc_fence_after();
             float sv[BN];
-            tmem_ld64(tS, *reinterpret_cast<float(*)[64]>(&sv[0]));
-            tmem_ld64(tS + 64, *reinterpret_cast<float(*)[64]>(&sv[64]));
+            tmem_ld64_async(tS, &sv[0]);
+            tmem_ld64_async(tS + 64, &sv[64]);
+            tmem_wait_ld128(sv);
             const int k0 = u * BN;
             if (SOFTCAP || ALIBI) {
                 // base-2 logits: cap * tanh(scale s / cap) [+ slope (kj - qi)], times log2(e).
