@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(L):
     names = _declared_functions()
     for expected in ("attn_fwd", "attn_fwd_ex", "attn_decode", "attn_decode_workspace_size",
                      "gbattn_status_string", "gbattn_device_status", "gbattn_set_wait_timeout_ns",
-                     "gbattn_version", "gbattn_diag_umma"):
+                     "gbattn_version", "gbattn_diag_umma", "gbattn_diag_wait_timeout"):
         assert expected in names
     for n in names:
         assert hasattr(L, n), n
@@ -93,6 +93,11 @@ def test_decode_rejects_bad_arguments(L):
 
 def test_fwd_ex_null_params(L):
     assert L.attn_fwd_ex(None) == 1
+
+
+def test_diag_wait_timeout_rejects_bad_limits(L):
+    assert L.gbattn_diag_wait_timeout(0, None) == 1
+    assert L.gbattn_diag_wait_timeout(10_000_000_001, None) == 1
 
 
 def test_binding_refuses_cpu_tensors():

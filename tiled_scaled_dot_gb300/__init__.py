@@ -24,7 +24,7 @@ import threading
 import torch
 
 __all__ = ["attn_fwd", "attn_decode", "decode_workspace_size", "device_status", "set_wait_timeout_ns",
-           "diag_umma", "GbattnError", "lib", "LIB_PATH"]
+           "diag_umma", "diag_wait_timeout", "GbattnError", "lib", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgbattn.so")
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
             L.gbattn_version.restype = I
             L.gbattn_diag_umma.argtypes = [I, P, P, P, I, P]
             L.gbattn_diag_umma.restype = I
+            L.gbattn_diag_wait_timeout.argtypes = [ctypes.c_ulonglong, P]
+            L.gbattn_diag_wait_timeout.restype = I
             _lib = L
     return _lib
 
@@ -225,3 +227,11 @@ def diag_umma(mode: int, a, b, n: int, stream=None):
     if st:
         raise GbattnError(st, "gbattn_diag_umma")
     return c
+
+
+def diag_wait_timeout(timeout_ns: int, stream=None) -> None:
+    """Launch a bounded wait that nothing satisfies (see gbattn_diag.h); it
+    gives up after timeout_ns and sets bit 16 of the device status word."""
+    st = lib().gbattn_diag_wait_timeout(int(timeout_ns), _stream_handle(stream))
+    if st:
+        raise GbattnError(st, "gbattn_diag_wait_timeout")

@@ -52,22 +52,6 @@ EncodeTiledFn encode_fn() {
 }
 
 // Per-device facts (current device): status word address and SM count.
-bool device_facts(unsigned int** status, int* num_sms) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_status_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return false;
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-        g_status_ptr[dev] = static_cast<unsigned int*>(p);
-        g_num_sms[dev] = sms;
-    }
-    *status = g_status_ptr[dev];
-    *num_sms = g_num_sms[dev];
-    return true;
-}
 
 // Small cache of encoded tensor maps keyed by (device, pointer, extents, box).
 struct MapKey {
@@ -129,6 +113,23 @@ int check_common(int B, int Hq, int Hkv, int S, int Sk, int D, float scale, floa
 }
 
 }  // namespace
+
+bool device_facts(unsigned int** status, int* num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return false;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+        g_num_sms[dev] = sms;
+    }
+    *status = g_status_ptr[dev];
+    *num_sms = g_num_sms[dev];
+    return true;
+}
 
 bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
                         uint32_t box_rows) {

@@ -13,12 +13,11 @@ namespace gbattn {
 
 namespace {
 
-__device__ unsigned int g_diag_status;
-
 template <int N, int MODE>
 __global__ void __launch_bounds__(128, 1)
     diag_umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __nv_bfloat16* a_glob, float* c, unsigned long long timeout_ns) {
+                     const __nv_bfloat16* a_glob, float* c, unsigned int* status,
+                     unsigned long long timeout_ns) {
     constexpr int A_BYTES = 128 * 128 * 2;
     constexpr int B_BYTES = 128 * N * 2;
     extern __shared__ __align__(1024) uint8_t dyn_smem[];
@@ -44,7 +43,7 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base;
-    WaitCtl wc{&abort_flag, &g_diag_status, timeout_ns};
+    WaitCtl wc{&abort_flag, status, timeout_ns};
 
     if (threadIdx.x == 0) {
         mbar_arrive_expect_tx(&load_bar, A_BYTES + B_BYTES);
@@ -122,13 +121,33 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 template <int N, int MODE>
-cudaError_t run_diag(const CUtensorMap& ta, const CUtensorMap& tb, const void* a, float* c, cudaStream_t s) {
+cudaError_t run_diag(const CUtensorMap& ta, const CUtensorMap& tb, const void* a, float* c, unsigned int* status,
+                     cudaStream_t s) {
     auto k = diag_umma_kernel<N, MODE>;
     const int smem = 128 * 128 * 2 + 128 * N * 2 + 1024;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<1, 128, smem, s>>>(ta, tb, static_cast<const __nv_bfloat16*>(a), c, 2000000000ull);
+    k<<<1, 128, smem, s>>>(ta, tb, static_cast<const __nv_bfloat16*>(a), c, status, 2000000000ull);
     return cudaGetLastError();
+}
+
+// A wait that nothing satisfies: thread 0 waits, with the kernels' bounded
+// wait, on an mbarrier that no thread or copy ever arrives at.  When
+// timeout_ns has passed the wait sets ST_DIAG in the device status word and
+// the kernel returns; nothing else is touched.
+__global__ void __launch_bounds__(32, 1) diag_wait_kernel(unsigned int* status, unsigned long long timeout_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) {
+        WaitCtl wc{&abort_flag, status, timeout_ns};
+        (void)mbar_wait(&bar, 0, wc, ST_DIAG);
+    }
 }
 
 }  // namespace
@@ -143,14 +162,26 @@ extern "C" int gbattn_diag_umma(int mode, const void* a, const void* b, float* c
     if (!encode_map_bf16_3d(&ta, a, 128, 128, 1, 128)) return GBATTN_ERR_CUDA;
     const bool ok = mode == 0 ? encode_map_bf16_3d(&tb, b, 128, n, 1, n) : encode_map_bf16_3d(&tb, b, n, 128, 1, 128);
     if (!ok) return GBATTN_ERR_CUDA;
+    unsigned int* st = nullptr;
+    int sms = 0;
+    if (!device_facts(&st, &sms)) return GBATTN_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (n == 128) {
-        e = mode == 0 ? run_diag<128, 0>(ta, tb, a, c, s)
-                      : (mode == 1 ? run_diag<128, 1>(ta, tb, a, c, s) : run_diag<128, 2>(ta, tb, a, c, s));
+        e = mode == 0 ? run_diag<128, 0>(ta, tb, a, c, st, s)
+                      : (mode == 1 ? run_diag<128, 1>(ta, tb, a, c, st, s) : run_diag<128, 2>(ta, tb, a, c, st, s));
     } else {
-        e = mode == 0 ? run_diag<64, 0>(ta, tb, a, c, s)
-                      : (mode == 1 ? run_diag<64, 1>(ta, tb, a, c, s) : run_diag<64, 2>(ta, tb, a, c, s));
+        e = mode == 0 ? run_diag<64, 0>(ta, tb, a, c, st, s)
+                      : (mode == 1 ? run_diag<64, 1>(ta, tb, a, c, st, s) : run_diag<64, 2>(ta, tb, a, c, st, s));
     }
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+extern "C" int gbattn_diag_wait_timeout(unsigned long long timeout_ns, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > 10000000000ull) return GBATTN_ERR_INVALID_ARG;
+    unsigned int* st = nullptr;
+    int sms = 0;
+    if (!device_facts(&st, &sms)) return GBATTN_ERR_CUDA;
+    diag_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st, timeout_ns);
+    return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }

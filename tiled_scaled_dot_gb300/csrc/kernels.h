@@ -69,6 +69,10 @@ cudaError_t launch_prefill_f32(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream);
 
+// Device address of the library's status word and the SM count of the current
+// device (looked up once per device).  False if the CUDA runtime fails.
+bool device_facts(unsigned int** status, int* num_sms);
+
 // Decode split choice shared by attn_decode and attn_decode_workspace_size.
 void decode_split_plan(int B, int Hkv, int Sk, int num_sms, int requested, int* num_splits, int* chunk);
 
