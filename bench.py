@@ -301,6 +301,7 @@ def bench_decode(g, args, ws, dev, pk):
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                         "frac": round(gbs / pk["hbm"], 4), "traffic": ncu_traffic("decode", w.name),
                         "peak_source": f"hbm_gbs ({pk['source']})", "frac_of_8tbs_nominal": round(gbs / 8000.0, 4)}}
+    res["graph"] = decode_graph_timing(fn, args, ws, stream)
     if not args.no_e2e:
         qh = x["q"].cpu().pin_memory()
         kh = x["k"].cpu().pin_memory()
@@ -321,6 +322,30 @@ def bench_decode(g, args, ws, dev, pk):
                       "h2d_bytes_per_step": qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2,
                       "d2h_bytes_per_step": oh.numel() * 2, "ms_per_step": round(per2, 4)}
     return res
+
+
+def decode_graph_timing(fn, args, ws, stream, per_graph=10):
+    """The decode step replayed from a CUDA graph of `per_graph` steps (the
+    same calls, so host launch overhead is the only difference from eager)."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn(0)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(per_graph):
+                fn(i)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = max(2, args.steps // per_graph)
+        ms = max_over_ranks(time_region(lambda i: graph.replay(), reps, ws, stream), ws)
+        return {"ms_per_step": round(ms / (reps * per_graph), 4), "steps_per_graph": per_graph, "replays": reps}
+    except Exception as e:  # reported, never hidden
+        torch.cuda.synchronize()
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
