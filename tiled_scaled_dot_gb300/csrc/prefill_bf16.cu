@@ -65,6 +65,12 @@ constexpr int LAUNCH_REGS = 128;          // 65536 / 512
 // one commit.  NG group barriers cycle; a slot is refilled only after the
 // group that last used it was released, at most NS groups back, so NG >= NS.
 constexpr int NG = 8;
+// Work items are decoded once, by the producer warp, and published through a
+// ring of NI entries in shared memory (one full and one empty barrier each);
+// every thread of the MMA warp, the softmax and the epilogue warpgroups
+// releases an entry after copying it.
+constexpr int NI = 4;
+constexpr int ITEM_READERS = 32 + 2 * 128 + 128;
 
 template <int D>
 struct Cfg {
@@ -193,12 +199,28 @@ struct Smem {
     uint64_t q_full[2], q_empty[2];
     uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], l_full[2];
     uint64_t grp_full[NG], grp_empty[NG];  // one per step group of K/V tiles
+    uint64_t item_full[NI], item_empty[NI];
     uint64_t drain;
+    Slot item_slot[NI][2];
+    int item_end[NI];       // 1: no item left (the ring's last entry)
     float l_buf[2][2][BM];  // [item parity][slot][row]: softmax denominator l
     float m_buf[2][2][BM];  // running max (base 2) for lse
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// The k-th work item of this CTA as published by the producer warp.  Returns
+// 1 with the item's slots, 0 when no item is left, -1 if the wait gave up.
+// The entry is released as soon as it is copied.
+__device__ __forceinline__ int read_item(Smem& sm, int k, const WaitCtl& wc, uint32_t site, Slot (&s)[2]) {
+    const int i = k % NI;
+    if (!mbar_wait(&sm.item_full[i], (uint32_t)(k / NI) & 1u, wc, site)) return -1;
+    const int end = sm.item_end[i];
+    s[0] = sm.item_slot[i][0];
+    s[1] = sm.item_slot[i][1];
+    mbar_arrive(&sm.item_empty[i]);
+    return end ? 0 : 1;
+}
 
 // ---------------------------------------------------------------------------- softmax role
 template <int D, bool SOFTCAP, bool ALIBI>
@@ -210,14 +232,13 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128u * x;
     const uint32_t tO = tmem + lane_off + C::O_COL + D * x;
-    const int grid = gridDim.x, cta = blockIdx.x;
     uint32_t s_cnt = 0, l_cnt = 0;
     const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
     for (int k = 0;; ++k) {
-        const int item = item_of(k, cta, grid);
-        if (item >= p.n_items) break;
         Slot s[2];
-        decode_item(p, item, s);
+        const int got = read_item(sm, k, wc, ST_PREFILL_SOFTMAX, s);
+        if (!__all_sync(0xffffffffu, got >= 0)) return;
+        if (got == 0) break;
         const Slot sl = s[x];
         if (!slot_live(sl)) continue;  // unused or fully-masked tile: the epilogue writes zeros
         const int qi = sl.t * BM + r;
@@ -255,11 +276,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
                 }
             }
             if (k0 < ra || k0 + BN - 1 > rb) {
+                // admissible keys of the tile: lo <= j <= hi (none when lo > hi)
+                const int lo = ra - k0, hi = rb - k0;
 #pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    const int kj = k0 + j;
-                    sv[j] = (kj < ra || kj > rb) ? -INFINITY : sv[j];
-                }
+                for (int j = 0; j < BN; ++j) sv[j] = (j < lo || j > hi) ? -INFINITY : sv[j];
             }
             // row max over the tile: 8 independent chains of three-input max
             float mx[8];
@@ -337,15 +357,14 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
     using C = Cfg<D>;
     const int r = threadIdx.x & (BM - 1);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int grid = gridDim.x, cta = blockIdx.x;
     const bool issuer = (threadIdx.x & (BM - 1)) == 0;
     uint8_t* srow = stage + r * 128;
     uint32_t cnt[2] = {0, 0};
     for (int k = 0;; ++k) {
-        const int item = item_of(k, cta, grid);
-        if (item >= p.n_items) break;
         Slot s[2];
-        decode_item(p, item, s);
+        const int got = read_item(sm, k, wc, ST_PREFILL_EPILOGUE, s);
+        if (!__all_sync(0xffffffffu, got >= 0)) return;
+        if (got == 0) break;
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
             const Slot sl = s[x];
@@ -443,6 +462,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&sm.grp_full[i], 1);
             mbar_init(&sm.grp_empty[i], 1);
         }
+        for (int i = 0; i < NI; ++i) {
+            mbar_init(&sm.item_full[i], 1);
+            mbar_init(&sm.item_empty[i], ITEM_READERS);
+        }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_mbar_init();
@@ -481,9 +504,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int k = 0;; ++k) {
                 const int item = item_of(k, cta, grid);
-                if (item >= p.n_items) break;
+                const bool more = item < p.n_items;
                 Slot s[2];
-                decode_item(p, item, s);
+                if (more) decode_item(p, item, s);
+                {
+                    // publish the item (or the end of the list) to the other roles
+                    const int i = k % NI;
+                    const bool free_entry =
+                        k < NI || mbar_wait(&sm.item_empty[i], (uint32_t)(k / NI - 1) & 1u, wc, ST_PREFILL_PRODUCER);
+                    if (!__all_sync(0xffffffffu, free_entry)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        if (more) {
+                            sm.item_slot[i][0] = s[0];
+                            sm.item_slot[i][1] = s[1];
+                        }
+                        sm.item_end[i] = more ? 0 : 1;
+                        mbar_arrive(&sm.item_full[i]);
+                    }
+                }
+                if (!more) break;
                 if (lane == 0) {
                     const int hkv = s[0].h / p.G;
 #pragma unroll
@@ -571,10 +613,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
             const uint32_t sKVa = smem_u32(sKV);
             for (int k = 0;; ++k) {
-                const int item = item_of(k, cta, grid);
-                if (item >= p.n_items) break;
                 Slot s[2];
-                decode_item(p, item, s);
+                const int got = read_item(sm, k, wc, ST_PREFILL_MMA, s);
+                if (!__all_sync(0xffffffffu, got >= 0)) {
+                    ok = false;
+                    break;
+                }
+                if (got == 0) break;
                 {
                     int ulo = 0x7fffffff, uhi = -1;
 #pragma unroll
