@@ -162,7 +162,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "b3c329451ce86a4e"): 129104128,
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "2a5caa08642b62e7"): 128801792,
+    # decode: full-size one-pass capture, printed to three significant figures
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "618bfb227641ba53"): 2169430000,
 }
 
 
@@ -299,7 +301,8 @@ def bench_decode(g, args, ws, dev, pk):
            "launches_per_step": 2 if ws_bytes else 1, "gpu_launches": args.steps * (2 if ws_bytes else 1),
            "splits": int(splits),
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                        "frac": round(gbs / pk["hbm"], 4), "traffic": ncu_traffic("decode", w.name),
+                        "frac": round(gbs / pk["hbm"], 4),
+                        "traffic": None if args.decode_b else ncu_traffic("decode", w.name),
                         "peak_source": f"hbm_gbs ({pk['source']})", "frac_of_8tbs_nominal": round(gbs / 8000.0, 4)}}
     res["graph"] = decode_graph_timing(fn, args, ws, stream)
     if not args.no_e2e:
