@@ -275,11 +275,20 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
                     sv[j] = t;
                 }
             }
+            // admissible keys of the tile: lo <= j <= hi (none when lo > hi);
+            // with no lower bound in the tile for any row of the warp (causal
+            // masks) one compare per key suffices.  The vote is taken by the
+            // whole warp, before the per-row branch.
+            const int lo = ra - k0, hi = rb - k0;
+            const bool no_lower = __all_sync(0xffffffffu, lo <= 0);
             if (k0 < ra || k0 + BN - 1 > rb) {
-                // admissible keys of the tile: lo <= j <= hi (none when lo > hi)
-                const int lo = ra - k0, hi = rb - k0;
+                if (no_lower) {
 #pragma unroll
-                for (int j = 0; j < BN; ++j) sv[j] = (j < lo || j > hi) ? -INFINITY : sv[j];
+                    for (int j = 0; j < BN; ++j) sv[j] = (j > hi) ? -INFINITY : sv[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < BN; ++j) sv[j] = (j < lo || j > hi) ? -INFINITY : sv[j];
+                }
             }
             // row max over the tile: 8 independent chains of three-input max
             float mx[8];
