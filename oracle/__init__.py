@@ -12,9 +12,14 @@ section 3) in float64 and exists to cross-check the first.  Decode is the same
 definition with one query row and no causal mask ("gfx942 unified attention",
 section 4, last paragraph), so ``decode`` calls ``attn`` with Sq = 1.
 
-Parity pins: every function here is pinned by tests/test_oracle_pins.py
-(closed forms, brute force, library special cases, invariants); none is
-"parity unpinned".
+``attn_paged`` is paged-cache attention (attention.fkc.md,
+"attention_paged_naive"): keys and values read through a per-sequence block
+table from a pool [num_blocks, block_size, Hkv, D], per-sequence context
+lengths, and the implicit causal mask at the query's absolute position.
+
+Parity pins: every function here is pinned by tests/test_oracle_pins.py and
+tests/test_oracle_paged.py (closed forms, brute force, library special cases,
+invariants); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -160,3 +165,70 @@ def decode(q, k, v, *, scale=None, softcap=None, alibi_slopes=None, rows=None, t
         raise ValueError("decode takes Sq == 1")
     return attn(q, k, v, scale=scale, causal=False, softcap=softcap, alibi_slopes=alibi_slopes,
                 rows=rows, threads=threads, return_lse=return_lse)
+
+
+def attn_paged(q, k_cache, v_cache, block_table, context_lens, *, scale=None, softcap=None,
+               alibi_slopes=None, return_lse=False):
+    """Paged-cache attention in float64 (attention.fkc.md, "attention_paged_naive").
+
+    q [B, Hq, Sq, D]; k_cache, v_cache [num_blocks, block_size, Hkv, D];
+    block_table [B, max_blocks] and context_lens [B] (non-negative integers).
+    For each (b, h, q_pos) the logical keys are k_pos = 0 .. context_lens[b] - 1,
+    key k_pos living at pool block block_table[b, k_pos // block_size], row
+    k_pos % block_size, kv head h // (Hq / Hkv).  The query's absolute position
+    is abs_pos = max(context_lens[b] - Sq, 0) + q_pos (the saturating
+    subtraction of the contract); keys after it are masked.  Scores: scale q.k,
+    then softcap c tanh(s / c), then + slope_h (k_pos - abs_pos); a stable
+    softmax and the weighted sum of V rows.  A row with no admissible key is
+    the zero row with lse = -inf.  A physical block index >= num_blocks is an
+    error (ValueError), as in the contract.  Returns float64 out [B, Hq, Sq, D]
+    (and lse [B, Hq, Sq]).
+    """
+    q = q.detach().to("cpu", torch.float64)
+    K = k_cache.detach().to("cpu", torch.float64)
+    V = v_cache.detach().to("cpu", torch.float64)
+    bt = block_table.detach().to("cpu", torch.int64)
+    cl = context_lens.detach().to("cpu", torch.int64)
+    if q.dim() != 4 or K.dim() != 4 or K.shape != V.shape:
+        raise ValueError("q [B,Hq,Sq,D], pools [num_blocks, block_size, Hkv, D]")
+    B, Hq, Sq, D = q.shape
+    nblk, bs, Hkv, Dk = K.shape
+    if Dk != D or Hq % Hkv or bt.dim() != 2 or bt.shape[0] != B or tuple(cl.shape) != (B,):
+        raise ValueError("shape mismatch")
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    sc = _f32(scale)
+    cap = 0.0 if not softcap else _f32(softcap)
+    slopes = None if alibi_slopes is None else alibi_slopes.detach().to("cpu", torch.float32).double()
+    out = torch.zeros(B, Hq, Sq, D, dtype=torch.float64)
+    lse = torch.full((B, Hq, Sq), float("-inf"), dtype=torch.float64)
+    for b in range(B):
+        ctx = int(cl[b])
+        if ctx > bt.shape[1] * bs:
+            raise ValueError("context length beyond the block table")
+        pos = torch.arange(ctx, dtype=torch.int64)
+        blk = bt[b, pos // bs] if ctx else torch.zeros(0, dtype=torch.int64)
+        if ctx and (int(blk.min()) < 0 or int(blk.max()) >= nblk):
+            raise ValueError("physical block index out of range")
+        off = pos % bs
+        Kb, Vb = K[blk, off], V[blk, off]  # [ctx, Hkv, D]: the gathered keys in logical order
+        abs_pos = max(ctx - Sq, 0) + torch.arange(Sq, dtype=torch.int64)  # [Sq]
+        admissible = pos[None, :] <= abs_pos[:, None]  # [Sq, ctx]
+        for h in range(Hq):
+            g = h // G
+            s = sc * (q[b, h] @ Kb[:, g, :].T)  # [Sq, ctx]
+            if cap:
+                s = cap * torch.tanh(s / cap)
+            if slopes is not None:
+                s = s + slopes[h] * (pos[None, :] - abs_pos[:, None]).double()
+            s = torch.where(admissible, s, torch.full_like(s, float("-inf")))
+            for i in range(Sq):
+                m = s[i].max() if ctx else torch.tensor(float("-inf"), dtype=torch.float64)
+                if m == float("-inf"):
+                    continue
+                w = torch.exp(s[i] - m)
+                L = w.sum()
+                out[b, h, i] = (w @ Vb[:, g, :]) / L
+                lse[b, h, i] = m + torch.log(L)
+    return (out, lse) if return_lse else out

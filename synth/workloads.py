@@ -112,3 +112,35 @@ def scaled(w: Workload, **changes) -> Workload:
     d = {f: getattr(w, f) for f in w.__dataclass_fields__}
     d.update(changes)
     return Workload(**d)
+
+
+STREAM_PAGED = 4  # block placement and context lengths of paged inputs
+
+
+def make_paged_inputs(B: int, Hq: int, Hkv: int, D: int, context_lens, block_size: int, dtype=torch.bfloat16,
+                      device="cpu", seed: int = 0, spare_blocks: int = 3, max_blocks: int | None = None,
+                      Sq: int = 1) -> dict:
+    """Seeded paged-cache inputs: q [B, Hq, Sq, D]; k_cache / v_cache
+    [num_blocks, block_size, Hkv, D] N(0,1); a block table [B, max_blocks]
+    (int32) that places every sequence's blocks at seeded, shuffled physical
+    positions of the pool (plus `spare_blocks` unused ones); context_lens [B]
+    (int32).  Table entries past a sequence's last block hold num_blocks + 7,
+    which no reader may dereference."""
+    from . import uniform
+    ctx = [int(c) for c in context_lens]
+    nb = [(c + block_size - 1) // block_size for c in ctx]
+    mb = max(max(nb), 1) if max_blocks is None else max_blocks
+    num_blocks = sum(nb) + spare_blocks
+    perm = torch.argsort(uniform(seed, STREAM_PAGED, 0, num_blocks))  # a seeded shuffle of the pool
+    table = torch.full((B, mb), num_blocks + 7, dtype=torch.int32)
+    i = 0
+    for b in range(B):
+        for j in range(nb[b]):
+            table[b, j] = int(perm[i])
+            i += 1
+    q = normal((B, Hq, Sq, D), seed, STREAM_Q, dtype, device)
+    k = normal((num_blocks, block_size, Hkv, D), seed, STREAM_K, dtype, device)
+    v = normal((num_blocks, block_size, Hkv, D), seed, STREAM_V, dtype, device)
+    return dict(q=q, k_cache=k, v_cache=v, block_table=table.to(device),
+                context_lens=torch.tensor(ctx, dtype=torch.int32, device=device), num_blocks=num_blocks,
+                block_size=block_size)
