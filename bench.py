@@ -6,7 +6,10 @@ A step is one pass of the hot path over one batch of synthetic input:
     Hkv=8, S=2048, D=128 (tile loads, Q K^T, masks, online softmax, P V,
     normalisation and store, all in one kernel launch), inputs resident in HBM;
   * decode (reported beside it): attn_decode on bf16 B=64, Hq=32, Hkv=8,
-    Sk=8192, D=128 (split-KV partials and the log-sum-exp combine).
+    Sk=8192, D=128 (split-KV partials and the log-sum-exp combine);
+  * paged decode (reported beside it): attn_decode_paged on the same heads
+    with seeded contexts of 4096..8192 keys in 64-token blocks of a shuffled
+    pool.
 value = causal-adjusted attention TFLOP/s (4 D flops per admissible
 (query, key) pair) over all ranks.  The decode object reports HBM GB/s of its
 algorithmic bytes (Q + K + V + O).
@@ -54,7 +57,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
-    ap.add_argument("--profile", choices=["prefill", "decode", "both"], default=None,
+    ap.add_argument("--no-paged", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode", "both", "paged"], default=None,
                     help="launch warm-up + steps of one path and exit (for ncu); no timing, one input copy")
     ap.add_argument("--decode-b", type=int, default=None, help="override the decode batch (smaller ncu captures)")
     return ap.parse_args()
@@ -327,6 +331,54 @@ def bench_decode(g, args, ws, dev, pk):
     return res
 
 
+PAGED_SHAPE = dict(B=64, Hq=32, Hkv=8, D=128, block_size=64, ctx_lo=4096, ctx_hi=8192)
+
+
+def paged_workload_name():
+    c = PAGED_SHAPE
+    return (f"bf16_paged_decode_b{c['B']}_h{c['Hq']}_kv{c['Hkv']}_ctx{c['ctx_lo']}-{c['ctx_hi']}_"
+            f"bs{c['block_size']}_d{c['D']}")
+
+
+def bench_decode_paged(g, args, ws, dev, pk):
+    """Paged-cache decode (attn_decode_paged): seeded per-sequence contexts of
+    4096..8192 keys in 64-token blocks at shuffled pool positions.  GB/s of the
+    algorithmic bytes: K and V of every live context, plus Q and O."""
+    import synth
+    from synth.workloads import make_paged_inputs
+    c = PAGED_SHAPE
+    ctx = (c["ctx_lo"] + synth.randint(c["B"], c["ctx_hi"] - c["ctx_lo"] + 1, 0, 5)).tolist()
+    x = make_paged_inputs(c["B"], c["Hq"], c["Hkv"], c["D"], ctx, c["block_size"], device=dev)
+    out = torch.empty_like(x["q"])
+    wsb = g.decode_paged_workspace_size(c["B"], c["Hq"], c["Hkv"], x["block_table"].shape[1], c["block_size"],
+                                        c["D"], 0)
+    wsp = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+    fn = lambda i: g.attn_decode_paged(x["q"], x["k_cache"], x["v_cache"], x["block_table"], x["context_lens"],
+                                       out=out, workspace=wsp)
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    if args.profile:
+        for i in range(args.steps):
+            fn(i)
+        torch.cuda.synchronize()
+        return None
+    soak(fn, 0.5)
+    stream = torch.cuda.current_stream()
+    ms = max_over_ranks(time_region(fn, args.steps, ws, stream), ws)
+    per = ms / args.steps
+    nbytes = 2 * sum(ctx) * c["Hkv"] * c["D"] * 2 + 2 * c["B"] * c["Hq"] * c["D"] * 2
+    gbs = nbytes / (per * 1e-3) / 1e9
+    return {"workload": paged_workload_name(), "metric": "paged decode HBM GB/s (live K+V, Q, O bytes)",
+            "value": round(gbs * ws, 1), "unit": "GB/s", "ms_per_step": round(per, 4), "bytes_per_step": nbytes,
+            "gpu_launches": args.steps * (2 if wsb else 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm"], 4),
+                         "traffic": ncu_traffic("decode", paged_workload_name()),
+                         "peak_source": f"hbm_gbs ({pk['source']})", "frac_of_8tbs_nominal": round(gbs / 8000.0, 4)},
+            "graph": decode_graph_timing(fn, args, ws, stream)}
+
+
 def decode_graph_timing(fn, args, ws, stream, per_graph=10):
     """The decode step replayed from a CUDA graph of `per_graph` steps (the
     same calls, so host launch overhead is the only difference from eager)."""
@@ -434,6 +486,8 @@ def main():
             bench_prefill(g, w, args, ws, dev, pk)
         if args.profile in ("decode", "both"):
             bench_decode(g, args, ws, dev, pk)
+        if args.profile == "paged":
+            bench_decode_paged(g, args, ws, dev, pk)
         if g.device_status() != 0:
             raise RuntimeError("device status word set")
         if rank == 0:
@@ -444,6 +498,7 @@ def main():
     try:
         pre = bench_prefill(g, w, args, ws, dev, pk)
         dec = None if args.no_decode else bench_decode(g, args, ws, dev, pk)
+        paged = None if args.no_paged else bench_decode_paged(g, args, ws, dev, pk)
     finally:
         clocks = sampler.stop()
     if g.device_status() != 0:
@@ -467,6 +522,8 @@ def main():
         line["e2e"] = pre["e2e"]
     if dec is not None:
         line["decode"] = dec
+    if paged is not None:
+        line["decode_paged"] = paged
     if rank == 0 and not args.no_cpu_baseline:
         x_cpu = make_inputs(w, "cpu")
         tf, sample, threads = oracle_sample(w, x_cpu, args.cpu_seconds)

@@ -174,6 +174,44 @@ int attn_decode_noalloc(const void* q, const void* k, const void* v, const float
                         float* lse_out, int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap,
                         int num_splits, int dtype, void* stream);
 
+/*
+ * attn_decode_paged -- decode step over a paged KV cache (attention.fkc.md,
+ * "attention_paged_naive": a per-sequence block table over a blocked pool,
+ * per-sequence context lengths, the causal mask implicit at the query's
+ * absolute position).  One query row per (b, h) (Sq = 1): its keys are the
+ * logical positions k_pos = 0 .. context_lens[b] - 1, key k_pos living in pool
+ * block block_table[b, k_pos / block_size], row k_pos % block_size.  The query
+ * sits at abs_pos = context_lens[b] - 1, so every key of the context is
+ * admissible and the ALiBi term is slope_h * (k_pos - abs_pos).  A sequence
+ * with context length 0 outputs the zero row (lse -inf).  Split-KV over keys
+ * and the log-sum-exp combine as in attn_decode.
+ *
+ *  q              device [B, Hq, 1, D] bf16.
+ *  k_cache, v_cache  device pools [num_blocks, block_size, Hkv, D] bf16.
+ *  block_table    device uint32 [B, max_blocks_per_seq]; only the entries of
+ *                 blocks that hold keys of the context are read.
+ *  context_lens   device uint32 [B].
+ *  alibi_slopes   device fp32 [Hq] or NULL.
+ *  out            device [B, Hq, 1, D]; lse_out device fp32 [B, Hq] or NULL.
+ *  block_size     a power of two, 16 .. 1024.
+ *  num_splits, workspace  as in attn_decode, sized by
+ *                 attn_decode_paged_workspace_size (for the longest context
+ *                 the table can hold, max_blocks_per_seq * block_size).
+ *  dtype          GBATTN_BF16; D 64 or 128.
+ * The contract's bounds check of physical block indices happens on the device:
+ * an index >= num_blocks, or a context length above max_blocks_per_seq *
+ * block_size, sets bit 10 of the device status word (gbattn_device_status);
+ * the output is then unspecified.  Such keys are never read from outside the
+ * pool.
+ */
+size_t attn_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_blocks_per_seq, int block_size, int D,
+                                        int num_splits);
+int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const uint32_t* block_table,
+                      const uint32_t* context_lens, const float* alibi_slopes, void* out, float* lse_out, int B,
+                      int Hq, int Hkv, int D, int num_blocks, int block_size, int max_blocks_per_seq,
+                      float softmax_scale, float softcap, int num_splits, void* workspace, size_t workspace_bytes,
+                      int dtype, void* stream);
+
 /* Human-readable text of a status code (static storage). */
 const char* gbattn_status_string(int status);
 

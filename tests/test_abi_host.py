@@ -35,7 +35,8 @@ def test_every_declared_symbol_is_exported(L):
     names = _declared_functions()
     for expected in ("attn_fwd", "attn_fwd_ex", "attn_decode", "attn_decode_workspace_size",
                      "gbattn_status_string", "gbattn_device_status", "gbattn_set_wait_timeout_ns",
-                     "gbattn_version", "gbattn_diag_umma", "gbattn_diag_wait_timeout"):
+                     "gbattn_version", "gbattn_diag_umma", "gbattn_diag_wait_timeout",
+                     "attn_decode_paged", "attn_decode_paged_workspace_size"):
         assert expected in names
     for n in names:
         assert hasattr(L, n), n
@@ -106,3 +107,27 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         g.attn_fwd(q, q[:, :1], q[:, :1])
+
+
+def test_paged_decode_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    # q, k_cache, v_cache, block_table, context_lens, slopes, out, lse,
+    # B, Hq, Hkv, D, num_blocks, block_size, max_blocks, scale, softcap, splits, ws, ws_bytes, dtype, stream
+    base = [P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 5), P(FAKE * 6), None, P(FAKE * 4), None,
+            2, 4, 2, 128, 10, 64, 4, 0.1, 0.0, 1, None, 0, 0, None]
+    def call(i, val):
+        a = list(base)
+        a[i] = val
+        return L.attn_decode_paged(*a)
+    assert call(13, 48) == 1          # block size not a power of two
+    assert call(13, 8) == 1           # block size below 16
+    assert call(12, 0) == 1           # no blocks
+    assert call(14, 0) == 1           # empty table
+    assert call(3, None) == 1         # no block table
+    assert call(4, P(FAKE * 6 + 2)) == 1  # misaligned context lengths
+    assert call(11, 96) == 2          # D
+    assert call(20, 1) == 2           # fp32 not built
+    assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 48, 128, 0) == 0
+    assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 1) == 0
+    assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 2) == \
+        L.attn_decode_workspace_size(2, 4, 2, 256, 128, 2)

@@ -23,7 +23,8 @@ import threading
 
 import torch
 
-__all__ = ["attn_fwd", "attn_decode", "decode_workspace_size", "device_status", "set_wait_timeout_ns",
+__all__ = ["attn_fwd", "attn_decode", "decode_workspace_size", "attn_decode_paged",
+           "decode_paged_workspace_size", "device_status", "set_wait_timeout_ns",
            "diag_umma", "diag_wait_timeout", "GbattnError", "lib", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -72,6 +73,10 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_workspace_size.restype = Z
             L.attn_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, F, I, P, Z, I, P]
             L.attn_decode.restype = I
+            L.attn_decode_paged_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            L.attn_decode_paged_workspace_size.restype = Z
+            L.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, P, Z, I, P]
+            L.attn_decode_paged.restype = I
             L.gbattn_status_string.argtypes = [I]
             L.gbattn_status_string.restype = ctypes.c_char_p
             L.gbattn_device_status.argtypes = [P, I]
@@ -206,6 +211,56 @@ def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None,
                            _ptr(workspace), ws_bytes, GBATTN_BF16, _stream_handle(stream))
     if st:
         raise GbattnError(st, "attn_decode")
+    return out
+
+
+def decode_paged_workspace_size(B, Hq, Hkv, max_blocks_per_seq, block_size, D, num_splits=0) -> int:
+    return int(lib().attn_decode_paged_workspace_size(B, Hq, Hkv, max_blocks_per_seq, block_size, D, num_splits))
+
+
+def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slopes=None, *, softmax_scale=None,
+                      softcap=None, num_splits=0, out=None, lse=None, workspace=None, stream=None):
+    """Decode over a paged KV cache (see attn_decode_paged in gbattn.h).
+
+    q [B,Hq,1,D] bf16; k_cache / v_cache [num_blocks, block_size, Hkv, D] bf16;
+    block_table [B, max_blocks] and context_lens [B] int32 or uint32 (CUDA),
+    read as uint32.  Returns out [B,Hq,1,D].
+    """
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check(t, n, torch.bfloat16, 4)
+    for t, n in ((block_table, "block_table"), (context_lens, "context_lens")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CUDA tensor")
+        if t.dtype not in (torch.int32, torch.uint32):
+            raise ValueError(f"{n} must be int32 or uint32")
+    B, Hq, Sq, D = q.shape
+    num_blocks, block_size, Hkv, Dk = k_cache.shape
+    if Sq != 1:
+        raise ValueError("paged decode takes one query row (Sq == 1)")
+    if tuple(v_cache.shape) != tuple(k_cache.shape) or Dk != D:
+        raise ValueError("k_cache and v_cache must be [num_blocks, block_size, Hkv, D] with q's D")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(context_lens.shape) != (B,):
+        raise ValueError("block_table [B, max_blocks], context_lens [B]")
+    if alibi_slopes is not None:
+        _check(alibi_slopes, "alibi_slopes", torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 4)
+    if lse is not None:
+        _check(lse, "lse", torch.float32)
+    max_blocks = block_table.shape[1]
+    need = decode_paged_workspace_size(B, Hq, Hkv, max_blocks, block_size, D, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
+    st = lib().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(context_lens),
+                                 _ptr(alibi_slopes), _ptr(out), _ptr(lse), B, Hq, Hkv, D, num_blocks, block_size,
+                                 max_blocks, scale, float(softcap or 0.0), int(num_splits), _ptr(workspace),
+                                 ws_bytes, GBATTN_BF16, _stream_handle(stream))
+    if st:
+        raise GbattnError(st, "attn_decode_paged")
     return out
 
 

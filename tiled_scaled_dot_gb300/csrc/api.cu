@@ -56,12 +56,13 @@ EncodeTiledFn encode_fn() {
 // Small cache of encoded tensor maps keyed by (device, pointer, extents, box).
 struct MapKey {
     int dev;
+    int kind;  // 0: [planes][rows][cols] tiles, 1: paged pool [planes = tokens][rows = heads][cols]
     const void* base;
     uint64_t cols, rows, planes;
     uint32_t box_rows;
     bool operator==(const MapKey& o) const {
-        return dev == o.dev && base == o.base && cols == o.cols && rows == o.rows && planes == o.planes &&
-               box_rows == o.box_rows;
+        return dev == o.dev && kind == o.kind && base == o.base && cols == o.cols && rows == o.rows &&
+               planes == o.planes && box_rows == o.box_rows;
     }
 };
 constexpr int kCache = 32;
@@ -70,10 +71,10 @@ CUtensorMap g_maps[kCache];
 int g_used = 0, g_next = 0;
 
 bool cached_map(CUtensorMap* out, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
-                uint32_t box_rows) {
+                uint32_t box_rows, int kind = 0) {
     int dev = 0;
     cudaGetDevice(&dev);
-    MapKey key{dev, base, cols, rows, planes, box_rows};
+    MapKey key{dev, kind, base, cols, rows, planes, box_rows};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (int i = 0; i < g_used; ++i)
@@ -83,7 +84,9 @@ bool cached_map(CUtensorMap* out, const void* base, uint64_t cols, uint64_t rows
             }
     }
     CUtensorMap m;
-    if (!encode_map_bf16_3d(&m, base, cols, rows, planes, box_rows)) return false;
+    const bool ok = kind == 0 ? encode_map_bf16_3d(&m, base, cols, rows, planes, box_rows)
+                              : encode_map_pool_bf16(&m, base, cols, rows, planes, box_rows);
+    if (!ok) return false;
     std::lock_guard<std::mutex> lk(g_mu);
     int slot = g_used < kCache ? g_used++ : (g_next++ % kCache);
     g_keys[slot] = key;
@@ -138,6 +141,19 @@ bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint6
     cuuint64_t dims[3] = {cols, rows, planes};
     cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
     cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_map_pool_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t heads, uint64_t rows,
+                          uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cols, heads, rows};
+    cuuint64_t strides[2] = {cols * 2, cols * heads * 2};
+    cuuint32_t box[3] = {64, 1, box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -290,6 +306,84 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
     f.timeout_ns = g_timeout_ns;
     CUtensorMap tk, tv;
     if (!cached_map(&tk, k, D, Sk, (uint64_t)B * Hkv, 64) || !cached_map(&tv, v, D, Sk, (uint64_t)B * Hkv, 64))
+        return GBATTN_ERR_CUDA;
+    cudaError_t e = launch_decode_bf16(f, tk, tv, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+static bool paged_geometry(int block_size, int max_blocks, int num_blocks, int* max_ctx) {
+    if (block_size < 16 || block_size > 1024 || (block_size & (block_size - 1))) return false;
+    if (max_blocks <= 0 || num_blocks <= 0) return false;
+    const long long mc = (long long)max_blocks * block_size, pool = (long long)num_blocks * block_size;
+    if (mc > 0x7fffffffLL || pool >= 0x7fffffffLL) return false;
+    *max_ctx = (int)mc;
+    return true;
+}
+
+size_t attn_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_blocks_per_seq, int block_size, int D,
+                                        int num_splits) {
+    int max_ctx = 0;
+    if (!paged_geometry(block_size, max_blocks_per_seq, 1, &max_ctx)) return 0;
+    return attn_decode_workspace_size(B, Hq, Hkv, max_ctx, D, num_splits);
+}
+
+int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const uint32_t* block_table,
+                      const uint32_t* context_lens, const float* alibi_slopes, void* out, float* lse_out, int B,
+                      int Hq, int Hkv, int D, int num_blocks, int block_size, int max_blocks_per_seq,
+                      float softmax_scale, float softcap, int num_splits, void* workspace, size_t workspace_bytes,
+                      int dtype, void* stream) {
+    int max_ctx = 0;
+    if (!paged_geometry(block_size, max_blocks_per_seq, num_blocks, &max_ctx)) return GBATTN_ERR_INVALID_ARG;
+    int rc = check_common(B, Hq, Hkv, 1, max_ctx, D, softmax_scale, softcap, dtype);
+    if (rc) return rc;
+    if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+    if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out || num_splits < 0)
+        return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return GBATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(context_lens)) & 3u)
+        return GBATTN_ERR_INVALID_ARG;
+    if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    const size_t nq = (size_t)B * Hq * D * 2, npool = (size_t)num_blocks * block_size * Hkv * D * 2;
+    if (overlaps(out, nq, q, nq) || overlaps(out, nq, k_cache, npool) || overlaps(out, nq, v_cache, npool))
+        return GBATTN_ERR_INVALID_ARG;
+
+    DecodeProblem f{};
+    if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
+    decode_split_plan(B, Hkv, max_ctx, f.num_sms, num_splits, &f.num_splits, &f.chunk);
+    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, max_ctx, D, num_splits);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GBATTN_ERR_INVALID_ARG;
+        if (overlaps(workspace, need, out, nq) || overlaps(workspace, need, q, nq) ||
+            overlaps(workspace, need, k_cache, npool) || overlaps(workspace, need, v_cache, npool))
+            return GBATTN_ERR_INVALID_ARG;
+        f.ws_o = static_cast<float*>(workspace);
+        f.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + (size_t)B * Hq * f.num_splits * D * 4);
+    }
+    f.q = q;
+    f.k = k_cache;
+    f.v = v_cache;
+    f.slopes = alibi_slopes;
+    f.out = out;
+    f.lse = lse_out;
+    f.B = B;
+    f.Hq = Hq;
+    f.Hkv = Hkv;
+    f.Sk = max_ctx;
+    f.D = D;
+    f.scale = softmax_scale;
+    f.softcap = softcap;
+    f.timeout_ns = g_timeout_ns;
+    f.paged = 1;
+    f.block_table = block_table;
+    f.context_lens = context_lens;
+    f.max_blocks = max_blocks_per_seq;
+    f.block_size = block_size;
+    f.num_blocks = num_blocks;
+    const uint32_t box = block_size < 64 ? (uint32_t)block_size : 64u;
+    const uint64_t rows = (uint64_t)num_blocks * block_size;
+    CUtensorMap tk, tv;
+    if (!cached_map(&tk, k_cache, D, Hkv, rows, box, 1) || !cached_map(&tv, v_cache, D, Hkv, rows, box, 1))
         return GBATTN_ERR_CUDA;
     cudaError_t e = launch_decode_bf16(f, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;

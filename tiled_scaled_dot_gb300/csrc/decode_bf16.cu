@@ -50,6 +50,10 @@ struct DecParams {
     int n_tiles;        // tiles over Sk
     float qscale;       // multiplies q: scale * log2(e) (no softcap) or scale (softcap)
     float softcap;
+    // paged cache: tile t of sequence b gathers keys [64 t, 64 t + 64) block by block
+    const uint32_t* block_table;   // [B, max_blocks]
+    const uint32_t* context_lens;  // [B]
+    int max_blocks, bs_log2, num_blocks;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -67,7 +71,7 @@ struct DCfg {
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled slab.
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-template <int D, int GC, bool SOFTCAP, bool ALIBI>
+template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const DecParams p) {
@@ -92,8 +96,17 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     rem /= p.n_chunks;
     const int hkv = rem % p.Hkv;
     const int b = rem / p.Hkv;
+    // Keys of this sequence: all Sk, or (paged cache) its context length,
+    // capped at what the block table can hold.  The query's absolute position
+    // for ALiBi is 0 (contiguous) or len - 1 (paged: the last position).
+    int len = p.Sk;
+    if (PAGED) {
+        const uint32_t c = __ldg(p.context_lens + b);
+        len = c > (uint32_t)p.Sk ? p.Sk : (int)c;
+        if (c > (uint32_t)p.Sk && threadIdx.x == 0 && split == 0 && hc == 0) atomicOr(p.status, ST_DECODE_PAGED_RANGE);
+    }
     const int t_begin = split * p.chunk_tiles;
-    const int t_end = min(p.n_tiles, t_begin + p.chunk_tiles);
+    const int t_end = min(PAGED ? (len + TILE - 1) / TILE : p.n_tiles, t_begin + p.chunk_tiles);
     const int h0 = hkv * p.G + hc * GC;                     // first query head of this chunk
     const int n_heads = min(GC, p.G - hc * GC);
 
@@ -123,10 +136,33 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
                 mbar_arrive_expect_tx(&full_bar[st], C::STAGE_BYTES);
                 uint8_t* ks = ring + st * C::STAGE_BYTES;
                 uint8_t* vs = ks + C::TILE_BYTES;
+                if (PAGED) {
+                    // one load per block (block_size < 64) or per 64 rows of a block;
+                    // keys past the context and bad block indices load from past the
+                    // pool's end, which reads zeros (the keys are masked anyway)
+                    const int rpl = min(1 << p.bs_log2, TILE);
+                    for (int i = 0; i < TILE / rpl; ++i) {
+                        const int kp = t * TILE + i * rpl;
+                        int z = p.num_blocks << p.bs_log2;
+                        if (kp < len) {
+                            const uint32_t blk = __ldg(p.block_table + (size_t)b * p.max_blocks + (kp >> p.bs_log2));
+                            if (blk < (uint32_t)p.num_blocks)
+                                z = ((int)blk << p.bs_log2) + (kp & ((1 << p.bs_log2) - 1));
+                            else
+                                atomicOr(p.status, ST_DECODE_PAGED_RANGE);
+                        }
 #pragma unroll
-                for (int sl = 0; sl < C::SLABS; ++sl) {
-                    tma_load_3d(ks + sl * C::SLAB, &tmK, &full_bar[st], sl * 64, t * TILE, plane);
-                    tma_load_3d(vs + sl * C::SLAB, &tmV, &full_bar[st], sl * 64, t * TILE, plane);
+                        for (int sl = 0; sl < C::SLABS; ++sl) {
+                            tma_load_3d(ks + sl * C::SLAB + i * rpl * 128, &tmK, &full_bar[st], sl * 64, hkv, z);
+                            tma_load_3d(vs + sl * C::SLAB + i * rpl * 128, &tmV, &full_bar[st], sl * 64, hkv, z);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int sl = 0; sl < C::SLABS; ++sl) {
+                        tma_load_3d(ks + sl * C::SLAB, &tmK, &full_bar[st], sl * 64, t * TILE, plane);
+                        tma_load_3d(vs + sl * C::SLAB, &tmV, &full_bar[st], sl * 64, t * TILE, plane);
+                    }
                 }
             }
             if (!ok) {
@@ -245,8 +281,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
                 const float e = ex2_approx(x * (2.f * LOG2E / p.softcap));
                 x = p.softcap * LOG2E * (1.f - 2.f / (e + 1.f));
             }
-            if (ALIBI) x = fmaf(slope_l2, (float)kj, x);
-            if (kj >= p.Sk) x = -INFINITY;
+            if (ALIBI) x = fmaf(slope_l2, (float)(PAGED ? kj - (len - 1) : kj), x);
+            if (kj >= len) x = -INFINITY;
             sv[ps] = x;
             mt = fmaxf(mt, x);
         }
@@ -371,9 +407,9 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
     if (lse && d == 0) lse[row] = (L > 0.f) ? (M + log2f(L)) * lse_to_natural : -INFINITY;
 }
 
-template <int D, int GC, bool SOFTCAP, bool ALIBI>
+template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED>
 cudaError_t launch_dec(const DecParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-    auto kern = decode_bf16_kernel<D, GC, SOFTCAP, ALIBI>;
+    auto kern = decode_bf16_kernel<D, GC, SOFTCAP, ALIBI, PAGED>;
     const int smem = DCfg<D>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -386,11 +422,21 @@ cudaError_t launch_dec(const DecParams& p, const CUtensorMap& tk, const CUtensor
     return cudaGetLastError();
 }
 
+template <int D, int GC, bool PAGED>
+cudaError_t launch_dec_caps(const DecParams& p, bool cap, bool ali, const CUtensorMap& tk, const CUtensorMap& tv,
+                            cudaStream_t s) {
+    if (cap)
+        return ali ? launch_dec<D, GC, true, true, PAGED>(p, tk, tv, s)
+                   : launch_dec<D, GC, true, false, PAGED>(p, tk, tv, s);
+    return ali ? launch_dec<D, GC, false, true, PAGED>(p, tk, tv, s)
+               : launch_dec<D, GC, false, false, PAGED>(p, tk, tv, s);
+}
+
 template <int D, int GC>
-cudaError_t launch_dec_flags(const DecParams& p, bool cap, bool ali, const CUtensorMap& tk, const CUtensorMap& tv,
-                             cudaStream_t s) {
-    if (cap) return ali ? launch_dec<D, GC, true, true>(p, tk, tv, s) : launch_dec<D, GC, true, false>(p, tk, tv, s);
-    return ali ? launch_dec<D, GC, false, true>(p, tk, tv, s) : launch_dec<D, GC, false, false>(p, tk, tv, s);
+cudaError_t launch_dec_flags(const DecParams& p, bool cap, bool ali, bool paged, const CUtensorMap& tk,
+                             const CUtensorMap& tv, cudaStream_t s) {
+    return paged ? launch_dec_caps<D, GC, true>(p, cap, ali, tk, tv, s)
+                 : launch_dec_caps<D, GC, false>(p, cap, ali, tk, tv, s);
 }
 
 }  // namespace
@@ -442,22 +488,32 @@ cudaError_t launch_decode_bf16(const DecodeProblem& f, const CUtensorMap& tk, co
     p.chunk_tiles = f.chunk / TILE;
     p.n_tiles = (f.Sk + TILE - 1) / TILE;
     p.softcap = f.softcap;
+    const bool paged = f.paged != 0;
+    if (paged) {
+        p.block_table = f.block_table;
+        p.context_lens = f.context_lens;
+        p.max_blocks = f.max_blocks;
+        p.num_blocks = f.num_blocks;
+        int lg = 0;
+        while ((1 << lg) < f.block_size) ++lg;
+        p.bs_log2 = lg;
+    }
     const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
     p.qscale = cap ? f.scale : f.scale * LOG2E;
     const int G = p.G;
     if (f.D == 128) {
         const int GC = G >= 4 ? 4 : (G == 3 ? 4 : (G == 2 ? 2 : 1));
         p.n_chunks = (G + GC - 1) / GC;
-        if (GC == 4) return launch_dec_flags<128, 4>(p, cap, ali, tk, tv, stream);
-        if (GC == 2) return launch_dec_flags<128, 2>(p, cap, ali, tk, tv, stream);
-        return launch_dec_flags<128, 1>(p, cap, ali, tk, tv, stream);
+        if (GC == 4) return launch_dec_flags<128, 4>(p, cap, ali, paged, tk, tv, stream);
+        if (GC == 2) return launch_dec_flags<128, 2>(p, cap, ali, paged, tk, tv, stream);
+        return launch_dec_flags<128, 1>(p, cap, ali, paged, tk, tv, stream);
     }
     const int GC = G >= 5 ? 8 : (G >= 3 ? 4 : (G == 2 ? 2 : 1));
     p.n_chunks = (G + GC - 1) / GC;
-    if (GC == 8) return launch_dec_flags<64, 8>(p, cap, ali, tk, tv, stream);
-    if (GC == 4) return launch_dec_flags<64, 4>(p, cap, ali, tk, tv, stream);
-    if (GC == 2) return launch_dec_flags<64, 2>(p, cap, ali, tk, tv, stream);
-    return launch_dec_flags<64, 1>(p, cap, ali, tk, tv, stream);
+    if (GC == 8) return launch_dec_flags<64, 8>(p, cap, ali, paged, tk, tv, stream);
+    if (GC == 4) return launch_dec_flags<64, 4>(p, cap, ali, paged, tk, tv, stream);
+    if (GC == 2) return launch_dec_flags<64, 2>(p, cap, ali, paged, tk, tv, stream);
+    return launch_dec_flags<64, 1>(p, cap, ali, paged, tk, tv, stream);
 }
 
 }  // namespace gbattn

@@ -44,6 +44,12 @@ struct DecodeProblem {
     unsigned int* status;
     unsigned long long timeout_ns;
     int num_sms;
+    // paged cache (k, v are pools [num_blocks, block_size, Hkv, D]); Sk is the
+    // longest context the block table can hold (max_blocks * block_size)
+    int paged;
+    const uint32_t* block_table;   // [B, max_blocks]
+    const uint32_t* context_lens;  // [B]
+    int max_blocks, block_size, num_blocks;
 };
 
 // Bits of the device status word: which wait gave up.
@@ -54,6 +60,7 @@ enum : unsigned int {
     ST_PREFILL_EPILOGUE = 1u << 3,
     ST_DECODE_PRODUCER = 1u << 8,
     ST_DECODE_CONSUMER = 1u << 9,
+    ST_DECODE_PAGED_RANGE = 1u << 10,  // a physical block index >= num_blocks, or a context past the table
     ST_DIAG = 1u << 16,
 };
 
@@ -61,6 +68,12 @@ enum : unsigned int {
 // a {64, box_rows, 1} box and 128-byte swizzle; out-of-range rows read as 0.
 bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
                         uint32_t box_rows);
+
+// 3-D bf16 tensor map over a paged pool [rows][heads][cols] (rows = num_blocks *
+// block_size tokens) with a {64, 1, box_rows} box and 128-byte swizzle: one
+// box is box_rows consecutive tokens of one head; rows past the pool read as 0.
+bool encode_map_pool_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t heads, uint64_t rows,
+                          uint32_t box_rows);
 
 // Kernel launchers.  Each returns the launch's cudaError_t.
 cudaError_t launch_prefill_bf16(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,
