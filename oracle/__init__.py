@@ -17,8 +17,14 @@ section 4, last paragraph), so ``decode`` calls ``attn`` with Sq = 1.
 table from a pool [num_blocks, block_size, Hkv, D], per-sequence context
 lengths, and the implicit causal mask at the query's absolute position.
 
-Parity pins: every function here is pinned by tests/test_oracle_pins.py and
-tests/test_oracle_paged.py (closed forms, brute force, library special cases,
+``attn_varlen`` is attention over packed variable-length sequences
+("gfx942 unified attention", section 5: queries packed [total_q, heads, D]
+with a cu_seqlens_q prefix sum, seqused_k per sequence) with the causal mask
+aligned bottom-right (section 4): query i of a sequence sits at absolute
+position kv_len - q_len + i.
+
+Parity pins: every function here is pinned by tests/test_oracle_pins.py,
+tests/test_oracle_varlen.py and tests/test_oracle_paged.py (closed forms, brute force, library special cases,
 invariants); none is "parity unpinned".
 """
 from __future__ import annotations
@@ -231,4 +237,79 @@ def attn_paged(q, k_cache, v_cache, block_table, context_lens, *, scale=None, so
                 L = w.sum()
                 out[b, h, i] = (w @ Vb[:, g, :]) / L
                 lse[b, h, i] = m + torch.log(L)
+    return (out, lse) if return_lse else out
+
+
+def attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, seqused_k=None, scale=None, causal=False,
+                window_left=None, window_right=None, softcap=None, alibi_slopes=None, return_lse=False):
+    """Packed variable-length attention in float64.
+
+    q [total_q, Hq, D], k / v [total_k, Hkv, D]; cu_seqlens_q / cu_seqlens_k
+    [B + 1] prefix sums; seqused_k [B] (optional) the live keys of each
+    sequence, a prefix of its cu_seqlens_k range.  For sequence b with q_len
+    queries and kv_len live keys, query i sits at abs_i = kv_len - q_len + i
+    ("gfx942 unified attention", section 4: bottom-right alignment); key j
+    (0 .. kv_len - 1) is admissible iff (not causal or j <= abs_i) and
+    (window_left is None or j >= abs_i - window_left) and (window_right is
+    None or j <= abs_i + window_right).  Scores: scale q.k, softcap
+    c tanh(s / c), + slope_h (j - abs_i); stable softmax; weighted V.  A row
+    with no admissible key is the zero row, lse -inf.  Returns float64 out
+    [total_q, Hq, D] (and lse [Hq, total_q]).
+    """
+    q = q.detach().to("cpu", torch.float64)
+    k = k.detach().to("cpu", torch.float64)
+    v = v.detach().to("cpu", torch.float64)
+    cq = [int(x) for x in cu_seqlens_q.detach().to("cpu").tolist()]
+    ck = [int(x) for x in cu_seqlens_k.detach().to("cpu").tolist()]
+    B = len(cq) - 1
+    if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or len(ck) != B + 1:
+        raise ValueError("q [total_q, Hq, D], k / v [total_k, Hkv, D], cu_seqlens [B + 1]")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    if Dk != D or Hq % Hkv or cq[0] != 0 or ck[0] != 0 or cq[-1] != total_q or ck[-1] > total_k:
+        raise ValueError("shape mismatch")
+    if any(b < a for a, b in zip(cq, cq[1:])) or any(b < a for a, b in zip(ck, ck[1:])):
+        raise ValueError("cu_seqlens must be non-decreasing")
+    used = None if seqused_k is None else [int(x) for x in seqused_k.detach().to("cpu").tolist()]
+    G = Hq // Hkv
+    sc = _f32(1.0 / (D ** 0.5) if scale is None else scale)
+    cap = 0.0 if not softcap else _f32(softcap)
+    slopes = None if alibi_slopes is None else alibi_slopes.detach().to("cpu", torch.float32).double()
+    out = torch.zeros(total_q, Hq, D, dtype=torch.float64)
+    lse = torch.full((Hq, total_q), float("-inf"), dtype=torch.float64)
+    for b in range(B):
+        q_len = cq[b + 1] - cq[b]
+        kv_len = ck[b + 1] - ck[b]
+        if used is not None:
+            if not 0 <= used[b] <= kv_len:
+                raise ValueError("seqused_k must be within the sequence's keys")
+            kv_len = used[b]
+        if q_len == 0:
+            continue
+        j = torch.arange(kv_len, dtype=torch.int64)
+        abs_i = kv_len - q_len + torch.arange(q_len, dtype=torch.int64)
+        adm = torch.ones(q_len, kv_len, dtype=torch.bool)
+        if causal:
+            adm &= j[None, :] <= abs_i[:, None]
+        if window_left is not None and window_left >= 0:
+            adm &= j[None, :] >= abs_i[:, None] - window_left
+        if window_right is not None and window_right >= 0:
+            adm &= j[None, :] <= abs_i[:, None] + window_right
+        kb, vb = k[ck[b]:ck[b] + kv_len], v[ck[b]:ck[b] + kv_len]
+        for h in range(Hq):
+            g = h // G
+            s = sc * (q[cq[b]:cq[b + 1], h, :] @ kb[:, g, :].T)  # [q_len, kv_len]
+            if cap:
+                s = cap * torch.tanh(s / cap)
+            if slopes is not None:
+                s = s + slopes[h] * (j[None, :] - abs_i[:, None]).double()
+            s = torch.where(adm, s, torch.full_like(s, float("-inf")))
+            for i in range(q_len):
+                m = s[i].max() if kv_len else torch.tensor(float("-inf"), dtype=torch.float64)
+                if m == float("-inf"):
+                    continue
+                w = torch.exp(s[i] - m)
+                L = w.sum()
+                out[cq[b] + i, h] = (w @ vb[:, g, :]) / L
+                lse[h, cq[b] + i] = m + torch.log(L)
     return (out, lse) if return_lse else out
