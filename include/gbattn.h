@@ -119,6 +119,37 @@ typedef struct {
 int attn_fwd_ex(const gbattn_fwd_params* p);
 
 /*
+ * attn_fwd_varlen -- attention over packed variable-length sequences
+ * ("gfx942 unified attention", section 5: queries packed [total_q, heads, D]
+ * with a cu_seqlens_q prefix sum, seqused_k carrying each sequence's KV
+ * length; section 4: the causal mask aligned bottom-right).  Sequence b
+ * (0 <= b < B) has queries q[cu_seqlens_q[b] .. cu_seqlens_q[b+1]) and keys
+ * k, v[cu_seqlens_k[b] .. cu_seqlens_k[b+1]), of which the first
+ * seqused_k[b] are live (all of them when seqused_k is NULL).  With q_len
+ * queries and kv_len live keys, query i sits at position kv_len - q_len + i:
+ * causal admits keys j <= that position, window_left / window_right (-1 =
+ * none) bound j to [pos - window_left, pos + window_right], and ALiBi adds
+ * slope_h * (j - pos).  Rows with no admissible key are zero (lse -inf).
+ * Softcap and scale as in attn_fwd.
+ *
+ *  q, out         device bf16 [total_q, Hq, D]; k, v device bf16 [total_k, Hkv, D].
+ *  cu_seqlens_q, cu_seqlens_k  device int32 [B + 1], non-decreasing, from 0;
+ *                 cu_seqlens_q[B] = total_q, cu_seqlens_k[B] <= total_k.
+ *  seqused_k      device int32 [B] or NULL.
+ *  lse_out        device fp32 [Hq, total_q] (natural log) or NULL.
+ *  max_seqlen_q   at least every sequence's query count (sizes the work list).
+ *  dtype          GBATTN_BF16; D 64 or 128.
+ * Offsets or lengths outside the tensors (or a sequence longer than
+ * max_seqlen_q) are clamped on the device and set bit 4 of the device status
+ * word; the output is then unspecified.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, const int32_t* seqused_k, const float* alibi_slopes, void* out,
+                    float* lse_out, int B, int Hq, int Hkv, int D, int total_q, int total_k, int max_seqlen_q,
+                    float softmax_scale, int causal, int window_left, int window_right, float softcap, int dtype,
+                    void* stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device workspace attn_decode needs
  * for this problem and split count (num_splits = 0 picks the split count
  * attn_decode picks, for the current device).  Returns 0 for invalid sizes.

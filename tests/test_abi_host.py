@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(L):
     for expected in ("attn_fwd", "attn_fwd_ex", "attn_decode", "attn_decode_workspace_size",
                      "gbattn_status_string", "gbattn_device_status", "gbattn_set_wait_timeout_ns",
                      "gbattn_version", "gbattn_diag_umma", "gbattn_diag_wait_timeout",
-                     "attn_decode_paged", "attn_decode_paged_workspace_size"):
+                     "attn_decode_paged", "attn_decode_paged_workspace_size", "attn_fwd_varlen"):
         assert expected in names
     for n in names:
         assert hasattr(L, n), n
@@ -131,3 +131,26 @@ def test_paged_decode_rejects_bad_arguments(L):
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 1) == 0
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 2) == \
         L.attn_decode_workspace_size(2, 4, 2, 256, 128, 2)
+
+
+def test_varlen_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    # q, k, v, cu_q, cu_k, used_k, slopes, out, lse, B, Hq, Hkv, D, total_q, total_k, max_q,
+    # scale, causal, wl, wr, softcap, dtype, stream
+    base = [P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 5), P(FAKE * 6), None, None, P(FAKE * 4), None,
+            2, 4, 2, 128, 100, 100, 64, 0.1, 1, -1, -1, 0.0, 0, None]
+    def call(i, val):
+        a = list(base)
+        a[i] = val
+        return L.attn_fwd_varlen(*a)
+    assert call(13, 0) == 1           # total_q
+    assert call(14, 0) == 1           # total_k
+    assert call(15, 0) == 1           # max_seqlen_q
+    assert call(3, None) == 1         # cu_seqlens_q
+    assert call(5, P(FAKE * 7 + 2)) == 1  # misaligned seqused_k
+    assert call(10, 3) == 1           # Hq % Hkv
+    assert call(17, 2) == 1           # causal flag
+    assert call(18, -2) == 1          # window
+    assert call(12, 96) == 2          # D
+    assert call(21, 1) == 2           # fp32 not built
+    assert call(7, P(FAKE)) == 1      # out aliasing q

@@ -23,7 +23,7 @@ import threading
 
 import torch
 
-__all__ = ["attn_fwd", "attn_decode", "decode_workspace_size", "attn_decode_paged",
+__all__ = ["attn_fwd", "attn_fwd_varlen", "attn_decode", "decode_workspace_size", "attn_decode_paged",
            "decode_paged_workspace_size", "device_status", "set_wait_timeout_ns",
            "diag_umma", "diag_wait_timeout", "GbattnError", "lib", "LIB_PATH"]
 
@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_workspace_size.restype = Z
             L.attn_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, F, I, P, Z, I, P]
             L.attn_decode.restype = I
+            L.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F, I, P]
+            L.attn_fwd_varlen.restype = I
             L.attn_decode_paged_workspace_size.argtypes = [I, I, I, I, I, I, I]
             L.attn_decode_paged_workspace_size.restype = Z
             L.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, P, Z, I, P]
@@ -211,6 +213,46 @@ def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None,
                            _ptr(workspace), ws_bytes, GBATTN_BF16, _stream_handle(stream))
     if st:
         raise GbattnError(st, "attn_decode")
+    return out
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, seqused_k=None, alibi_slopes=None, *,
+                    softmax_scale=None, causal=False, window_left=None, window_right=None, softcap=None, out=None,
+                    lse=None, stream=None):
+    """Packed variable-length attention (see attn_fwd_varlen in gbattn.h).
+
+    q [total_q, Hq, D], k / v [total_k, Hkv, D] bf16; cu_seqlens_q / cu_seqlens_k
+    int32 [B + 1] and seqused_k int32 [B] (optional), all CUDA; max_seqlen_q an
+    int at least every sequence's query count.  Causal masks align bottom-right.
+    lse (optional) fp32 [Hq, total_q].  Returns out [total_q, Hq, D].
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, torch.bfloat16, 3)
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k"), (seqused_k, "seqused_k")):
+        if t is not None:
+            _check(t, n, torch.int32, 1)
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    B = cu_seqlens_q.shape[0] - 1
+    if tuple(v.shape) != tuple(k.shape) or Dk != D or cu_seqlens_k.shape[0] != B + 1:
+        raise ValueError("k and v must be [total_k, Hkv, D] with q's D; cu_seqlens_* must be [B + 1]")
+    if seqused_k is not None and seqused_k.shape[0] != B:
+        raise ValueError("seqused_k must be [B]")
+    if alibi_slopes is not None:
+        _check(alibi_slopes, "alibi_slopes", torch.float32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _check(lse, "lse", torch.float32)
+    scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
+    st = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(seqused_k),
+                               _ptr(alibi_slopes), _ptr(out), _ptr(lse), B, Hq, Hkv, D, total_q, total_k,
+                               int(max_seqlen_q), scale, 1 if causal else 0, _win(window_left), _win(window_right),
+                               float(softcap or 0.0), GBATTN_BF16, _stream_handle(stream))
+    if st:
+        raise GbattnError(st, "attn_fwd_varlen")
     return out
 
 

@@ -245,6 +245,64 @@ int attn_fwd(const void* q, const void* k, const void* v, const float* alibi_slo
     return attn_fwd_ex(&a);
 }
 
+int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* cu_seqlens_q,
+                    const int32_t* cu_seqlens_k, const int32_t* seqused_k, const float* alibi_slopes, void* out,
+                    float* lse_out, int B, int Hq, int Hkv, int D, int total_q, int total_k, int max_seqlen_q,
+                    float softmax_scale, int causal, int window_left, int window_right, float softcap, int dtype,
+                    void* stream) {
+    if (total_q <= 0 || total_k <= 0 || max_seqlen_q <= 0) return GBATTN_ERR_INVALID_ARG;
+    int rc = check_common(B, Hq, Hkv, max_seqlen_q, 1, D, softmax_scale, softcap, dtype);
+    if (rc) return rc;
+    if ((long long)total_q * Hq > 0x7fffffffLL || (long long)total_k * Hkv > 0x7fffffffLL)
+        return GBATTN_ERR_UNSUPPORTED;
+    if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return GBATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return GBATTN_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GBATTN_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) | reinterpret_cast<uintptr_t>(cu_seqlens_k) |
+         reinterpret_cast<uintptr_t>(seqused_k)) & 3u)
+        return GBATTN_ERR_INVALID_ARG;
+    if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    const size_t nq = (size_t)total_q * Hq * D * 2, nkv = (size_t)total_k * Hkv * D * 2;
+    if (overlaps(out, nq, q, nq) || overlaps(out, nq, k, nkv) || overlaps(out, nq, v, nkv))
+        return GBATTN_ERR_INVALID_ARG;
+
+    FwdProblem f{};
+    f.q = q;
+    f.k = k;
+    f.v = v;
+    f.slopes = alibi_slopes;
+    f.out = out;
+    f.lse = lse_out;
+    f.B = B;
+    f.Hq = Hq;
+    f.Hkv = Hkv;
+    f.Sq = max_seqlen_q;
+    f.Sk = 0;
+    f.D = D;
+    f.scale = softmax_scale;
+    f.causal = causal;
+    f.wl = window_left;
+    f.wr = window_right;
+    f.softcap = softcap;
+    f.timeout_ns = g_timeout_ns;
+    f.varlen = 1;
+    f.cu_q = cu_seqlens_q;
+    f.cu_k = cu_seqlens_k;
+    f.used_k = seqused_k;
+    f.total_q = total_q;
+    f.total_k = total_k;
+    if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
+    CUtensorMap tq, tk, tv, to;
+    if (!cached_map(&tq, q, D, Hq, total_q, 128, 1) || !cached_map(&tk, k, D, Hkv, total_k, 128, 1) ||
+        !cached_map(&tv, v, D, Hkv, total_k, 128, 1) || !cached_map(&to, out, D, Hq, total_q, 128, 1))
+        return GBATTN_ERR_CUDA;
+    cudaError_t e = launch_prefill_bf16(f, tq, tk, tv, to, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
 static int decode_plan(int B, int Hq, int Hkv, int Sk, int D, int num_splits, int* splits, int* chunk) {
     if (check_common(B, Hq, Hkv, 1, Sk, D, 1.f, 0.f, GBATTN_BF16)) return -1;
     if (num_splits < 0) return -1;

@@ -25,6 +25,13 @@ struct FwdProblem {
     unsigned int* status;       // device status word
     unsigned long long timeout_ns;
     int num_sms;
+    // packed variable-length sequences (q / out [total_q, Hq, D], k / v
+    // [total_k, Hkv, D]); Sq is then the longest sequence's query count
+    int varlen;
+    const int* cu_q;            // [B + 1]
+    const int* cu_k;            // [B + 1]
+    const int* used_k;          // [B] or nullptr
+    int total_q, total_k;
 };
 
 struct DecodeProblem {
@@ -58,6 +65,7 @@ enum : unsigned int {
     ST_PREFILL_MMA = 1u << 1,
     ST_PREFILL_SOFTMAX = 1u << 2,
     ST_PREFILL_EPILOGUE = 1u << 3,
+    ST_PREFILL_VARLEN_RANGE = 1u << 4,  // packed-sequence offsets / lengths outside the tensors
     ST_DECODE_PRODUCER = 1u << 8,
     ST_DECODE_CONSUMER = 1u << 9,
     ST_DECODE_PAGED_RANGE = 1u << 10,  // a physical block index >= num_blocks, or a context past the table

@@ -87,8 +87,8 @@ struct Cfg {
     // spilling at most a few bytes in any variant, the 184/64/80 split spilled
     // the epilogue and control loops
     static constexpr int SOFTMAX_REGS = 176;
-    static constexpr int EPI_REGS = 72;
-    static constexpr int CONTROL_REGS = 88;
+    static constexpr int EPI_REGS = 80;
+    static constexpr int CONTROL_REGS = 80;
     static_assert(2 * 128 * SOFTMAX_REGS + 128 * EPI_REGS + 128 * CONTROL_REGS <= NUM_THREADS * LAUNCH_REGS,
                   "register split");
 };
@@ -105,49 +105,104 @@ struct Params {
     float scale_log2;  // softmax_scale * log2(e)
     float cap_in;      // softmax_scale / softcap
     float cap_out;     // softcap * log2(e)
-    int n_qt;          // query tiles per head
+    int n_qt;          // query tiles per head (packed sequences: per sequence, at most)
     int pair_heads;    // 1: slots are heads (2p, 2p+1) at one row tile; 0: row tiles (2t, 2t+1) of one head
     int n_items;
+    // Packed variable-length sequences ("gfx942 unified attention", sections
+    // 4-5): q / out [total_q, Hq, D], k / v [total_k, Hkv, D]; sequence b's
+    // queries are rows cu_q[b] .. cu_q[b+1]-1, its live keys the first
+    // used_k[b] (or all) of rows cu_k[b] .. cu_k[b+1]-1; positions are aligned
+    // bottom-right (query i sits at k_len - q_len + i).
+    int varlen;
+    const int* cu_q;
+    const int* cu_k;
+    const int* used_k;
+    int total_q, total_k;
 };
 
 struct Slot {
-    int b, h, t;  // t < 0: slot unused in this item
-    int lo, hi;   // key-tile range, lo > hi: no admissible key for any row
+    int b, h, t;     // t < 0: slot unused in this item
+    int lo, hi;      // key-tile range, lo > hi: no admissible key for any row
+    int q0, q_len;   // the sequence's first query row (packed layout) and its queries
+    int k0, k_len;   // its first key row (packed layout) and its live keys
 };
 
-// Admissible key interval [a, e] of query row qi (a > e when empty).
-__device__ __forceinline__ void row_interval(const Params& p, int b, int qi, int& a, int& e) {
+// Position of query row i of a slot's sequence: i (dense problems, top-left)
+// or k_len - q_len + i (packed sequences, bottom-right).
+template <bool VARLEN>
+__device__ __forceinline__ int query_pos(const Slot& s, int i) {
+    return VARLEN ? s.k_len - s.q_len + i : i;
+}
+// Queries and keys of the slot's sequence.
+template <bool VARLEN>
+__device__ __forceinline__ int seq_q_len(const Params& p, const Slot& s) { return VARLEN ? s.q_len : p.Sq; }
+template <bool VARLEN>
+__device__ __forceinline__ int seq_k_len(const Params& p, const Slot& s) { return VARLEN ? s.k_len : p.Sk; }
+
+// Admissible key interval [a, e] of query row i of the slot's sequence (a > e when empty).
+template <bool VARLEN>
+__device__ __forceinline__ void row_interval(const Params& p, const Slot& s, int i, int& a, int& e) {
+    const int pos = query_pos<VARLEN>(s, i);
     a = 0;
-    e = p.Sk - 1;
-    if (p.causal) e = min(e, qi);
-    if (p.wl >= 0) a = max(a, qi - p.wl);
-    if (p.wr >= 0) e = min(e, qi + p.wr);
+    e = seq_k_len<VARLEN>(p, s) - 1;
+    if (p.causal) e = min(e, pos);
+    if (p.wl >= 0) a = max(a, pos - p.wl);
+    if (p.wr >= 0) e = min(e, pos + p.wr);
     if (p.rowb) {
-        int2 r = __ldg(p.rowb + (size_t)b * p.Sq + qi);
+        int2 r = __ldg(p.rowb + (size_t)s.b * p.Sq + i);
         a = max(a, r.x);
         e = min(e, r.y);
     }
 }
 
-// Item -> (b, h, t) of both slots, and each slot's key-tile range.  Called by
-// a whole warp (the range is a warp reduction over the slot's rows).
-__device__ __forceinline__ void decode_item(const Params& p, int item, Slot (&s)[2]) {
+// Item -> (b, h, t) of both slots, the sequence's geometry, and each slot's
+// key-tile range.  Called by a whole warp (the range is a warp reduction over
+// the slot's rows).  Returns false when neither slot has a query tile (a row
+// tile past a packed sequence's end).
+template <bool VARLEN>
+__device__ __forceinline__ bool decode_item(const Params& p, int item, Slot (&s)[2]) {
     const int lane = threadIdx.x & 31;
     if (p.pair_heads) {
         const int per_t = p.B * (p.Hq / 2);
         int tr = item / per_t, rest = item % per_t;
         int t = p.causal ? (p.n_qt - 1 - tr) : tr;
         int b = rest / (p.Hq / 2), pr = rest % (p.Hq / 2);
-        s[0] = Slot{b, 2 * pr, t, 0, -1};
-        s[1] = Slot{b, 2 * pr + 1, t, 0, -1};
+        s[0] = Slot{b, 2 * pr, t, 0, -1, 0, p.Sq, 0, p.Sk};
+        s[1] = Slot{b, 2 * pr + 1, t, 0, -1, 0, p.Sq, 0, p.Sk};
     } else {
         const int n_tp = (p.n_qt + 1) / 2;
         const int per_t = p.B * p.Hq;
         int tr = item / per_t, rest = item % per_t;
         int tp = p.causal ? (n_tp - 1 - tr) : tr;
         int b = rest / p.Hq, h = rest % p.Hq;
-        s[0] = Slot{b, h, 2 * tp, 0, -1};
-        s[1] = Slot{b, h, (2 * tp + 1 < p.n_qt) ? 2 * tp + 1 : -1, 0, -1};
+        s[0] = Slot{b, h, 2 * tp, 0, -1, 0, p.Sq, 0, p.Sk};
+        s[1] = Slot{b, h, (2 * tp + 1 < p.n_qt) ? 2 * tp + 1 : -1, 0, -1, 0, p.Sq, 0, p.Sk};
+    }
+    if (VARLEN) {
+        // the sequence's rows; offsets or lengths outside the tensors are
+        // clamped and reported in the status word
+        const int b = s[0].b;
+        int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
+        int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
+        int kl = p.used_k ? __ldg(p.used_k + b) : k1 - k0;
+        bool bad = q0 < 0 || q1 < q0 || q1 > p.total_q || k0 < 0 || k1 < k0 || k1 > p.total_k || kl < 0 ||
+                   kl > k1 - k0 || q1 - q0 > p.n_qt * BM;
+        if (bad) {
+            q0 = min(max(q0, 0), p.total_q);
+            q1 = min(max(q1, q0), min(p.total_q, q0 + p.n_qt * BM));
+            k0 = min(max(k0, 0), p.total_k);
+            k1 = min(max(k1, k0), p.total_k);
+            kl = min(max(kl, 0), k1 - k0);
+            if (lane == 0) atomicOr(p.status, ST_PREFILL_VARLEN_RANGE);
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            s[x].q0 = q0;
+            s[x].q_len = q1 - q0;
+            s[x].k0 = k0;
+            s[x].k_len = kl;
+            if (s[x].t * BM >= s[x].q_len) s[x].t = -1;
+        }
     }
 #pragma unroll
     for (int x = 0; x < 2; ++x) {
@@ -156,9 +211,9 @@ __device__ __forceinline__ void decode_item(const Params& p, int item, Slot (&s)
         const int q0 = s[x].t * BM;
         for (int r = lane; r < BM; r += 32) {
             int qi = q0 + r;
-            if (qi >= p.Sq) break;
+            if (qi >= seq_q_len<VARLEN>(p, s[x])) break;
             int a, e;
-            row_interval(p, s[x].b, qi, a, e);
+            row_interval<VARLEN>(p, s[x], qi, a, e);
             if (a <= e) {
                 kmin = min(kmin, a);
                 kmax = max(kmax, e);
@@ -174,6 +229,7 @@ __device__ __forceinline__ void decode_item(const Params& p, int item, Slot (&s)
             s[x].hi = kmax / BN;
         }
     }
+    return s[0].t >= 0 || s[1].t >= 0;
 }
 
 __device__ __forceinline__ int item_of(int k, int cta, int grid) {
@@ -223,7 +279,7 @@ __device__ __forceinline__ int read_item(Smem& sm, int k, const WaitCtl& wc, uin
 }
 
 // ---------------------------------------------------------------------------- softmax role
-template <int D, bool SOFTCAP, bool ALIBI>
+template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN>
 __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t tmem, const WaitCtl& wc,
                                              int warp) {
     using C = Cfg<D>;
@@ -241,9 +297,10 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
         if (got == 0) break;
         const Slot sl = s[x];
         if (!slot_live(sl)) continue;  // unused or fully-masked tile: the epilogue writes zeros
-        const int qi = sl.t * BM + r;
+        const int i_row = sl.t * BM + r;            // query row within the sequence
+        const int qi = query_pos<VARLEN>(sl, i_row);  // its position (ALiBi)
         int ra = 1, rb = 0;
-        if (qi < p.Sq) row_interval(p, sl.b, qi, ra, rb);
+        if (i_row < seq_q_len<VARLEN>(p, sl)) row_interval<VARLEN>(p, sl, i_row, ra, rb);
         float slope_l2 = 0.f;
         if (ALIBI) slope_l2 = __ldg(p.slopes + sl.h) * LOG2E;
         float m_used = -INFINITY, l = 0.f;
@@ -355,7 +412,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
 }
 
 // ---------------------------------------------------------------------------- epilogue role
-template <int D>
+template <int D, bool VARLEN>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_t tmem, const WaitCtl& wc,
                                               int warp, uint8_t* stage, const CUtensorMap* tmO) {
     // Output rows go through a 128-row x 64-column bf16 staging tile in shared
@@ -378,16 +435,22 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
         for (int x = 0; x < 2; ++x) {
             const Slot sl = s[x];
             if (sl.t < 0) continue;
-            const int qi = sl.t * BM + r;
-            const bool live = qi < p.Sq;
-            const size_t row = ((size_t)sl.b * p.Hq + sl.h) * p.Sq + qi;
+            const int qi = sl.t * BM + r;  // query row within the sequence
+            const bool live = qi < seq_q_len<VARLEN>(p, sl);
+            // output row of this thread and its lse entry: dense [B, Hq, Sq, D] and
+            // [B, Hq, Sq], or packed [total_q, Hq, D] and [Hq, total_q]
+            const size_t orow = VARLEN ? (size_t)(sl.q0 + qi) * p.Hq + sl.h : ((size_t)sl.b * p.Hq + sl.h) * p.Sq + qi;
+            const size_t lrow = VARLEN ? (size_t)sl.h * p.total_q + sl.q0 + qi : orow;
+            // a packed tile that ends inside its sequence is written row by row: a
+            // tensor store would also write the next sequence's rows
+            const bool ragged = VARLEN && sl.t * BM + BM > sl.q_len;
             if (sl.lo > sl.hi) {
                 // No admissible key for any row of the tile: zero rows.
                 if (live) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.out + row * D);
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
 #pragma unroll
                     for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-                    if (p.lse) p.lse[row] = -INFINITY;
+                    if (p.lse) p.lse[lrow] = -INFINITY;
                 }
                 continue;
             }
@@ -404,8 +467,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf) {
                 // the staging tile is free once the previous store has read it
-                if (issuer) bulk_wait_group_read0();
-                asm volatile("bar.sync 1, %0;" ::"n"(BM) : "memory");
+                if (!ragged) {
+                    if (issuer) bulk_wait_group_read0();
+                    asm volatile("bar.sync 1, %0;" ::"n"(BM) : "memory");
+                }
 #pragma unroll
                 for (int c32 = 0; c32 < 2; ++c32) {
                     float ov[32];
@@ -423,23 +488,32 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
                         w.y = pack_bf16x2(ov[8 * i + 2] * inv_l, ov[8 * i + 3] * inv_l);
                         w.z = pack_bf16x2(ov[8 * i + 4] * inv_l, ov[8 * i + 5] * inv_l);
                         w.w = pack_bf16x2(ov[8 * i + 6] * inv_l, ov[8 * i + 7] * inv_l);
-                        *reinterpret_cast<uint4*>(srow + ((c ^ (r & 7)) << 4)) = w;
+                        if (ragged) {
+                            if (live) reinterpret_cast<uint4*>(p.out + orow * D + hf * 64)[c] = w;
+                        } else {
+                            *reinterpret_cast<uint4*>(srow + ((c ^ (r & 7)) << 4)) = w;
+                        }
                     }
                 }
-                fence_proxy_async_smem();
-                asm volatile("bar.sync 1, %0;" ::"n"(BM) : "memory");
-                if (issuer) {
-                    tma_store_3d(tmO, stage, hf * 64, sl.t * BM, sl.b * p.Hq + sl.h);
-                    bulk_commit_group();
+                if (!ragged) {
+                    fence_proxy_async_smem();
+                    asm volatile("bar.sync 1, %0;" ::"n"(BM) : "memory");
+                    if (issuer) {
+                        if (VARLEN)
+                            tma_store_3d(tmO, stage, hf * 64, sl.h, sl.q0 + sl.t * BM);
+                        else
+                            tma_store_3d(tmO, stage, hf * 64, sl.t * BM, sl.b * p.Hq + sl.h);
+                        bulk_commit_group();
+                    }
                 }
             }
-            if (live && p.lse) p.lse[row] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
+            if (live && p.lse) p.lse[lrow] = (l > 0.f) ? (m + log2f(l)) * LN2 : -INFINITY;
         }
     }
     if (issuer) bulk_wait_group0();
 }
 
-template <int D, bool SOFTCAP, bool ALIBI>
+template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -493,10 +567,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Each warpgroup executes one setmaxnreg, at one program point, before its roles split.
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::SOFTMAX_REGS));
-        softmax_role<D, SOFTCAP, ALIBI>(p, sm, tmem, wc, warp);
+        softmax_role<D, SOFTCAP, ALIBI, VARLEN>(p, sm, tmem, wc, warp);
     } else if (warp < 12) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::EPI_REGS));
-        epilogue_role<D>(p, sm, tmem, wc, warp, sStage, &tmO);
+        epilogue_role<D, VARLEN>(p, sm, tmem, wc, warp, sStage, &tmO);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::CONTROL_REGS));
         if (warp == WARP_PRODUCER) {
@@ -511,16 +585,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < C::NS; ++i) slot_grp[i] = -1;
             bool ok = true;
+            int pk = 0;  // items published so far (row tiles past a packed sequence's end are skipped)
             for (int k = 0;; ++k) {
                 const int item = item_of(k, cta, grid);
                 const bool more = item < p.n_items;
                 Slot s[2];
-                if (more) decode_item(p, item, s);
+                if (more && !decode_item<VARLEN>(p, item, s)) continue;
                 {
                     // publish the item (or the end of the list) to the other roles
-                    const int i = k % NI;
+                    const int i = pk % NI;
                     const bool free_entry =
-                        k < NI || mbar_wait(&sm.item_empty[i], (uint32_t)(k / NI - 1) & 1u, wc, ST_PREFILL_PRODUCER);
+                        pk < NI || mbar_wait(&sm.item_empty[i], (uint32_t)(pk / NI - 1) & 1u, wc, ST_PREFILL_PRODUCER);
+                    ++pk;
                     if (!__all_sync(0xffffffffu, free_entry)) {
                         ok = false;
                         break;
@@ -544,9 +620,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (!ok) break;
                         mbar_arrive_expect_tx(&sm.q_full[x], C::Q_BYTES);
 #pragma unroll
-                        for (int hf = 0; hf < C::HALVES; ++hf)
-                            tma_load_3d(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].t * BM,
-                                        s[x].b * p.Hq + s[x].h);
+                        for (int hf = 0; hf < C::HALVES; ++hf) {
+                            if (VARLEN)  // packed [total_q][Hq][D]
+                                tma_load_3d(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].h,
+                                            s[x].q0 + s[x].t * BM);
+                            else
+                                tma_load_3d(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].t * BM,
+                                            s[x].b * p.Hq + s[x].h);
+                        }
                         ++q_cnt[x];
                     }
                     int ulo = 0x7fffffff, uhi = -1;
@@ -583,10 +664,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const bool is_v = has_v && i == 0;
                             const int st = (ld_cnt + i) % C::NS;
                             uint8_t* dst = sKV + st * C::KV_BYTES;
+                            const int key = (is_v ? u : u - 1) * BN;
 #pragma unroll
-                            for (int hf = 0; hf < C::HALVES; ++hf)
-                                tma_load_3d(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64,
-                                            (is_v ? u : u - 1) * BN, s[0].b * p.Hkv + hkv);
+                            for (int hf = 0; hf < C::HALVES; ++hf) {
+                                if (VARLEN)  // packed [total_k][Hkv][D]
+                                    tma_load_3d(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64, hkv,
+                                                s[0].k0 + key);
+                                else
+                                    tma_load_3d(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64, key,
+                                                s[0].b * p.Hkv + hkv);
+                            }
                             slot_grp[st] = (int)grp_cnt;
                         }
                         ld_cnt += nl;
@@ -727,10 +814,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int D, bool SOFTCAP, bool ALIBI>
+template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN>
 cudaError_t launch_variant(const Params& prm, int grid, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
-    auto kern = prefill_bf16_kernel<D, SOFTCAP, ALIBI>;
+    auto kern = prefill_bf16_kernel<D, SOFTCAP, ALIBI, VARLEN>;
     const int smem = Cfg<D>::SMEM_BYTES;
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -742,6 +829,21 @@ cudaError_t launch_variant(const Params& prm, int grid, const CUtensorMap& tq, c
     if (e != cudaSuccess) return e;
     kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tk, tv, to, prm);
     return cudaGetLastError();
+}
+
+template <bool VARLEN>
+cudaError_t launch_flags(const Params& p, int grid, int D, bool cap, bool ali, const CUtensorMap& tq,
+                         const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
+    if (D == 128) {
+        if (cap) return ali ? launch_variant<128, true, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
+                            : launch_variant<128, true, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
+        return ali ? launch_variant<128, false, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
+                   : launch_variant<128, false, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
+    }
+    if (cap) return ali ? launch_variant<64, true, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
+                        : launch_variant<64, true, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
+    return ali ? launch_variant<64, false, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
+               : launch_variant<64, false, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
 }
 
 }  // namespace
@@ -767,6 +869,12 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
     p.scale_log2 = f.scale * LOG2E;
     p.cap_in = f.softcap > 0.f ? f.scale / f.softcap : 0.f;
     p.cap_out = f.softcap * LOG2E;
+    p.varlen = f.varlen;
+    p.cu_q = f.cu_q;
+    p.cu_k = f.cu_k;
+    p.used_k = f.used_k;
+    p.total_q = f.total_q;
+    p.total_k = f.total_k;
     p.n_qt = (f.Sq + BM - 1) / BM;
     p.pair_heads = (p.G % 2 == 0) ? 1 : 0;
     if (p.pair_heads)
@@ -775,16 +883,8 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
         p.n_items = ((p.n_qt + 1) / 2) * f.B * f.Hq;
     const int grid = p.n_items < f.num_sms ? p.n_items : f.num_sms;
     const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
-    if (f.D == 128) {
-        if (cap) return ali ? launch_variant<128, true, true>(p, grid, tq, tk, tv, to, stream)
-                            : launch_variant<128, true, false>(p, grid, tq, tk, tv, to, stream);
-        return ali ? launch_variant<128, false, true>(p, grid, tq, tk, tv, to, stream)
-                   : launch_variant<128, false, false>(p, grid, tq, tk, tv, to, stream);
-    }
-    if (cap) return ali ? launch_variant<64, true, true>(p, grid, tq, tk, tv, to, stream)
-                        : launch_variant<64, true, false>(p, grid, tq, tk, tv, to, stream);
-    return ali ? launch_variant<64, false, true>(p, grid, tq, tk, tv, to, stream)
-               : launch_variant<64, false, false>(p, grid, tq, tk, tv, to, stream);
+    return p.varlen ? launch_flags<true>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream)
+                    : launch_flags<false>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream);
 }
 
 }  // namespace gbattn
