@@ -9,7 +9,9 @@ A step is one pass of the hot path over one batch of synthetic input:
     Sk=8192, D=128 (split-KV partials and the log-sum-exp combine);
   * paged decode (reported beside it): attn_decode_paged on the same heads
     with seeded contexts of 4096..8192 keys in 64-token blocks of a shuffled
-    pool.
+    pool;
+  * varlen prefill (reported beside it): attn_fwd_varlen on 32 packed causal
+    sequences of seeded lengths 512..4096.
 value = causal-adjusted attention TFLOP/s (4 D flops per admissible
 (query, key) pair) over all ranks.  The decode object reports HBM GB/s of its
 algorithmic bytes (Q + K + V + O).
@@ -58,7 +60,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-paged", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "decode", "both", "paged"], default=None,
+    ap.add_argument("--no-varlen", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode", "both", "paged", "varlen"], default=None,
                     help="launch warm-up + steps of one path and exit (for ncu); no timing, one input copy")
     ap.add_argument("--decode-b", type=int, default=None, help="override the decode batch (smaller ncu captures)")
     return ap.parse_args()
@@ -379,6 +382,50 @@ def bench_decode_paged(g, args, ws, dev, pk):
             "graph": decode_graph_timing(fn, args, ws, stream)}
 
 
+VARLEN_SHAPE = dict(B=32, Hq=32, Hkv=8, D=128, len_lo=512, len_hi=4096)
+
+
+def varlen_workload_name():
+    c = VARLEN_SHAPE
+    return f"bf16_varlen_causal_b{c['B']}_h{c['Hq']}_kv{c['Hkv']}_len{c['len_lo']}-{c['len_hi']}_d{c['D']}"
+
+
+def bench_varlen(g, args, ws, dev, pk):
+    """Packed variable-length causal prefill (attn_fwd_varlen): 32 sequences
+    of seeded lengths 512..4096 (queries = keys), Hq 32, Hkv 8, D 128.
+    TFLOP/s of 4 D flops per admissible (query, key) pair."""
+    import synth
+    c = VARLEN_SHAPE
+    lens = (c["len_lo"] + synth.randint(c["B"], c["len_hi"] - c["len_lo"] + 1, 0, 7)).tolist()
+    cu = torch.tensor([0] + [sum(lens[:i + 1]) for i in range(len(lens))], dtype=torch.int32, device=dev)
+    T = int(cu[-1])
+    q = synth.normal((T, c["Hq"], c["D"]), 0, synth.STREAM_Q, torch.bfloat16, dev)
+    k = synth.normal((T, c["Hkv"], c["D"]), 0, synth.STREAM_K, torch.bfloat16, dev)
+    v = synth.normal((T, c["Hkv"], c["D"]), 0, synth.STREAM_V, torch.bfloat16, dev)
+    out = torch.empty_like(q)
+    fn = lambda i: g.attn_fwd_varlen(q, k, v, cu, cu, max(lens), causal=True, out=out)
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    if args.profile:
+        for i in range(args.steps):
+            fn(i)
+        torch.cuda.synchronize()
+        return None
+    soak(fn, 0.5)
+    stream = torch.cuda.current_stream()
+    ms = max_over_ranks(time_region(fn, args.steps, ws, stream), ws)
+    per = ms / args.steps
+    flops = 4.0 * c["D"] * c["Hq"] * sum(n * (n + 1) / 2 for n in lens)
+    tf = flops / (per * 1e-3) / 1e12
+    return {"workload": varlen_workload_name(), "metric": "varlen causal prefill TFLOP/s (causal-adj)",
+            "value": round(tf * ws, 2), "unit": "TFLOP/s", "ms_per_step": round(per, 4), "flops_per_step": flops,
+            "total_tokens": T, "gpu_launches": args.steps,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tf / pk["bf16"], 4), "traffic": ncu_traffic("prefill", varlen_workload_name()),
+                         "peak_source": f"bf16_tflops ({pk['source']}, burst)"}}
+
+
 def decode_graph_timing(fn, args, ws, stream, per_graph=10):
     """The decode step replayed from a CUDA graph of `per_graph` steps (the
     same calls, so host launch overhead is the only difference from eager)."""
@@ -488,6 +535,8 @@ def main():
             bench_decode(g, args, ws, dev, pk)
         if args.profile == "paged":
             bench_decode_paged(g, args, ws, dev, pk)
+        if args.profile == "varlen":
+            bench_varlen(g, args, ws, dev, pk)
         if g.device_status() != 0:
             raise RuntimeError("device status word set")
         if rank == 0:
@@ -499,6 +548,7 @@ def main():
         pre = bench_prefill(g, w, args, ws, dev, pk)
         dec = None if args.no_decode else bench_decode(g, args, ws, dev, pk)
         paged = None if args.no_paged else bench_decode_paged(g, args, ws, dev, pk)
+        varl = None if args.no_varlen else bench_varlen(g, args, ws, dev, pk)
     finally:
         clocks = sampler.stop()
     if g.device_status() != 0:
@@ -524,6 +574,8 @@ def main():
         line["decode"] = dec
     if paged is not None:
         line["decode_paged"] = paged
+    if varl is not None:
+        line["varlen"] = varl
     if rank == 0 and not args.no_cpu_baseline:
         x_cpu = make_inputs(w, "cpu")
         tf, sample, threads = oracle_sample(w, x_cpu, args.cpu_seconds)
