@@ -42,7 +42,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-_DT = {torch.bfloat16: 0, torch.float32: 1, torch.float64: 2}
+_DT = {torch.bfloat16: 0, torch.float32: 1, torch.float64: 2, torch.float16: 3}
 
 
 def build(force: bool = False) -> str:
@@ -85,7 +85,7 @@ def _ptr(t):
 
 def _prep(q, k, v, alibi_slopes, row_kv_bounds):
     if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DT:
-        raise TypeError("q, k, v must share one of bf16 / f32 / f64")
+        raise TypeError("q, k, v must share one of bf16 / f16 / f32 / f64")
     q, k, v = (t.detach().to("cpu").contiguous() for t in (q, k, v))
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4 or k.shape != v.shape:
         raise ValueError("q [B,Hq,Sq,D], k and v [B,Hkv,Sk,D]")

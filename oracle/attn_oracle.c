@@ -27,7 +27,7 @@
  * O[d] = sum_j w_j V[b,g,j,d] / L, lse = M + ln L.  A row with no finite score
  * is the all-zero row with lse = -inf (attention_naive, fully-masked rows).
  *
- * Inputs are read exactly as stored (bf16 and f32 widen exactly to f64); scale,
+ * Inputs are read exactly as stored (bf16, f16 and f32 widen exactly to f64); scale,
  * slopes and softcap are the fp32 numbers the GPU receives, widened.
  *
  * A second entry, oracle_attn_tiled, walks the same problem the way
@@ -45,7 +45,22 @@
 #include <omp.h>
 #endif
 
-enum { OR_BF16 = 0, OR_F32 = 1, OR_F64 = 2 };
+enum { OR_BF16 = 0, OR_F32 = 1, OR_F64 = 2, OR_F16 = 3 };
+
+/* IEEE 754 binary16: sign, 5-bit exponent with bias 15, 10-bit fraction;
+ * exponent 0 holds zeros and subnormals (2^-14 * f / 1024), exponent 31
+ * infinities and NaNs.  Every value is exact in double. */
+static double half_to_double(uint16_t h) {
+    const int sign = (h >> 15) & 1, e = (h >> 10) & 31, f = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + (double)f, e - 25);
+    return sign ? -v : v;
+}
 
 static double widen(int dtype, const void *base, int64_t i) {
     if (dtype == OR_BF16) {
@@ -54,6 +69,7 @@ static double widen(int dtype, const void *base, int64_t i) {
         memcpy(&f, &bits, sizeof f);
         return (double)f;
     }
+    if (dtype == OR_F16) return half_to_double(((const uint16_t *)base)[i]);
     if (dtype == OR_F32) return (double)((const float *)base)[i];
     return ((const double *)base)[i];
 }
@@ -124,7 +140,7 @@ static void naive_row(const problem *p, int b, int h, int qi, double *srow, doub
 static int check(const problem *p) {
     if (p->B <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->Sq <= 0 || p->Sk <= 0 || p->D <= 0) return -1;
     if (p->Hq % p->Hkv != 0) return -1;
-    if (p->dtype < OR_BF16 || p->dtype > OR_F64) return -1;
+    if (p->dtype < OR_BF16 || p->dtype > OR_F16) return -1;
     return 0;
 }
 

@@ -381,3 +381,18 @@ def test_rejects_bad_problems():
     k = torch.zeros(1, 2, 2, 4)
     with pytest.raises(ValueError):
         oracle.attn(q, k, k)
+
+
+def test_fp16_inputs_widen_exactly():
+    """fp16 inputs are read by the oracle's own binary16 decoding; it must
+    agree bitwise with the same values widened to float64 by torch, including
+    subnormals, zeros of both signs and the largest finite values."""
+    q = synth.normal((1, 2, 9, 16), 17, 0, torch.float16)
+    k = synth.normal((1, 1, 11, 16), 17, 1, torch.float16)
+    v = synth.normal((1, 1, 11, 16), 17, 2, torch.float16)
+    v[0, 0, 0, :4] = torch.tensor([6.0e-8, -0.0, 65504.0, -3.0e-5], dtype=torch.float16)
+    k[0, 0, 1, :2] = torch.tensor([1.0e-6, -6.1e-5], dtype=torch.float16)
+    for causal in (False, True):
+        a, la = oracle.attn(q, k, v, causal=causal, softcap=10.0, return_lse=True)
+        b, lb = oracle.attn(q.double(), k.double(), v.double(), causal=causal, softcap=10.0, return_lse=True)
+        assert torch.equal(a, b) and torch.equal(la, lb)
