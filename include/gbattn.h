@@ -54,7 +54,8 @@ extern "C" {
 /* Element type of q, k, v and out. */
 typedef enum {
     GBATTN_BF16 = 0, /* bfloat16 storage, fp32 accumulation, bf16 output (RNE)   */
-    GBATTN_F32 = 1   /* float32 storage and arithmetic (SIMT FFMA, no TF32)       */
+    GBATTN_F32 = 1,  /* float32 storage and arithmetic (SIMT FFMA, no TF32)       */
+    GBATTN_F16 = 2   /* float16 storage, fp32 accumulation, fp16 output (RNE)     */
 } gbattn_dtype;
 
 enum {
@@ -80,7 +81,8 @@ enum {
  *  causal         0 or 1.
  *  window_left, window_right   -1 = unbounded (None), else >= 0.
  *  softcap        0 = none, else finite and > 0.
- *  dtype          GBATTN_BF16 or GBATTN_F32.
+ *  dtype          GBATTN_BF16, GBATTN_F16 (tensor cores, fp32 accumulation)
+ *                 or GBATTN_F32 (SIMT).
  *  stream         cudaStream_t.
  */
 int attn_fwd(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, int B, int Hq,
@@ -138,7 +140,7 @@ int attn_fwd_ex(const gbattn_fwd_params* p);
  *  seqused_k      device int32 [B] or NULL.
  *  lse_out        device fp32 [Hq, total_q] (natural log) or NULL.
  *  max_seqlen_q   at least every sequence's query count (sizes the work list).
- *  dtype          GBATTN_BF16; D 64 or 128.
+ *  dtype          GBATTN_BF16 (others return GBATTN_ERR_UNSUPPORTED); D 64 or 128.
  * Offsets or lengths outside the tensors (or a sequence longer than
  * max_seqlen_q) are clamped on the device and set bit 4 of the device status
  * word; the output is then unspecified.
@@ -174,7 +176,7 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Sk, int D, int num
  *                 attn_decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits)
  *                 bytes, 16-byte aligned (may be NULL when that size is 0).
  *                 Its contents need no initialisation and are not preserved.
- *  dtype          GBATTN_BF16 (GBATTN_F32 returns GBATTN_ERR_UNSUPPORTED).
+ *  dtype          GBATTN_BF16 or GBATTN_F16 (GBATTN_F32 returns GBATTN_ERR_UNSUPPORTED).
  *  D              64 or 128.
  */
 int attn_decode(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, float* lse_out,
@@ -217,8 +219,8 @@ int attn_decode_noalloc(const void* q, const void* k, const void* v, const float
  * with context length 0 outputs the zero row (lse -inf).  Split-KV over keys
  * and the log-sum-exp combine as in attn_decode.
  *
- *  q              device [B, Hq, 1, D] bf16.
- *  k_cache, v_cache  device pools [num_blocks, block_size, Hkv, D] bf16.
+ *  q              device [B, Hq, 1, D] (bf16 or fp16, see dtype).
+ *  k_cache, v_cache  device pools [num_blocks, block_size, Hkv, D], same type.
  *  block_table    device uint32 [B, max_blocks_per_seq]; only the entries of
  *                 blocks that hold keys of the context are read.
  *  context_lens   device uint32 [B].
@@ -228,7 +230,7 @@ int attn_decode_noalloc(const void* q, const void* k, const void* v, const float
  *  num_splits, workspace  as in attn_decode, sized by
  *                 attn_decode_paged_workspace_size (for the longest context
  *                 the table can hold, max_blocks_per_seq * block_size).
- *  dtype          GBATTN_BF16; D 64 or 128.
+ *  dtype          GBATTN_BF16 or GBATTN_F16 (q, pools and out alike); D 64 or 128.
  * The contract's bounds check of physical block indices happens on the device:
  * an index >= num_blocks, or a context length above max_blocks_per_seq *
  * block_size, sets bit 10 of the device status word (gbattn_device_status);

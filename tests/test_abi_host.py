@@ -127,6 +127,7 @@ def test_paged_decode_rejects_bad_arguments(L):
     assert call(4, P(FAKE * 6 + 2)) == 1  # misaligned context lengths
     assert call(11, 96) == 2          # D
     assert call(20, 1) == 2           # fp32 not built
+    assert call(20, 3) == 1           # no such type
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 48, 128, 0) == 0
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 1) == 0
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 2) == \
@@ -153,4 +154,5 @@ def test_varlen_rejects_bad_arguments(L):
     assert call(18, -2) == 1          # window
     assert call(12, 96) == 2          # D
     assert call(21, 1) == 2           # fp32 not built
+    assert call(21, 2) == 2           # fp16 varlen not built
     assert call(7, P(FAKE)) == 1      # out aliasing q

@@ -32,7 +32,9 @@ LIB_PATH = os.path.join(_HERE, "libgbattn.so")
 
 GBATTN_BF16 = 0
 GBATTN_F32 = 1
-_DT = {torch.bfloat16: GBATTN_BF16, torch.float32: GBATTN_F32}
+GBATTN_F16 = 2
+_DT = {torch.bfloat16: GBATTN_BF16, torch.float32: GBATTN_F32, torch.float16: GBATTN_F16}
+_DT16 = {torch.bfloat16: GBATTN_BF16, torch.float16: GBATTN_F16}  # the decode entries
 
 
 class GbattnError(RuntimeError):
@@ -182,13 +184,15 @@ def decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits=0) -> int:
 
 def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None, num_splits=0, out=None,
                 lse=None, workspace=None, stream=None):
-    """Split-KV decode.  q [B,Hq,1,D], k/v [B,Hkv,Sk,D] bf16 (CUDA).
+    """Split-KV decode.  q [B,Hq,1,D], k/v [B,Hkv,Sk,D] bf16 or fp16 (CUDA).
 
     workspace: optional uint8 CUDA tensor of at least decode_workspace_size(...)
     bytes; allocated here (through torch) when None.  Returns out [B,Hq,1,D].
     """
+    if q.dtype not in _DT16:
+        raise TypeError(f"decode takes bf16 or fp16, got {q.dtype}")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, torch.bfloat16, 4)
+        _check(t, n, q.dtype, 4)
     B, Hq, Sq, D = q.shape
     Bk, Hkv, Sk, Dk = k.shape
     if Sq != 1:
@@ -200,7 +204,7 @@ def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None,
     if out is None:
         out = torch.empty_like(q)
     else:
-        _check(out, "out", torch.bfloat16, 4)
+        _check(out, "out", q.dtype, 4)
     if lse is not None:
         _check(lse, "lse", torch.float32)
     need = decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits)
@@ -210,7 +214,7 @@ def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None,
     scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
     st = lib().attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(alibi_slopes), _ptr(out), _ptr(lse),
                            B, Hq, Hkv, Sk, D, scale, float(softcap or 0.0), int(num_splits),
-                           _ptr(workspace), ws_bytes, GBATTN_BF16, _stream_handle(stream))
+                           _ptr(workspace), ws_bytes, _DT16[q.dtype], _stream_handle(stream))
     if st:
         raise GbattnError(st, "attn_decode")
     return out
@@ -264,12 +268,14 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slop
                       softcap=None, num_splits=0, out=None, lse=None, workspace=None, stream=None):
     """Decode over a paged KV cache (see attn_decode_paged in gbattn.h).
 
-    q [B,Hq,1,D] bf16; k_cache / v_cache [num_blocks, block_size, Hkv, D] bf16;
+    q [B,Hq,1,D] bf16 or fp16; k_cache / v_cache [num_blocks, block_size, Hkv, D] of the same type;
     block_table [B, max_blocks] and context_lens [B] int32 or uint32 (CUDA),
     read as uint32.  Returns out [B,Hq,1,D].
     """
+    if q.dtype not in _DT16:
+        raise TypeError(f"paged decode takes bf16 or fp16, got {q.dtype}")
     for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _check(t, n, torch.bfloat16, 4)
+        _check(t, n, q.dtype, 4)
     for t, n in ((block_table, "block_table"), (context_lens, "context_lens")):
         if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous CUDA tensor")
@@ -288,7 +294,7 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slop
     if out is None:
         out = torch.empty_like(q)
     else:
-        _check(out, "out", torch.bfloat16, 4)
+        _check(out, "out", q.dtype, 4)
     if lse is not None:
         _check(lse, "lse", torch.float32)
     max_blocks = block_table.shape[1]
@@ -300,7 +306,7 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slop
     st = lib().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(context_lens),
                                  _ptr(alibi_slopes), _ptr(out), _ptr(lse), B, Hq, Hkv, D, num_blocks, block_size,
                                  max_blocks, scale, float(softcap or 0.0), int(num_splits), _ptr(workspace),
-                                 ws_bytes, GBATTN_BF16, _stream_handle(stream))
+                                 ws_bytes, _DT16[q.dtype], _stream_handle(stream))
     if st:
         raise GbattnError(st, "attn_decode_paged")
     return out

@@ -57,11 +57,12 @@ EncodeTiledFn encode_fn() {
 struct MapKey {
     int dev;
     int kind;  // 0: [planes][rows][cols] tiles, 1: paged pool [planes = tokens][rows = heads][cols]
+    int f16;   // element type: 0 bf16, 1 fp16
     const void* base;
     uint64_t cols, rows, planes;
     uint32_t box_rows;
     bool operator==(const MapKey& o) const {
-        return dev == o.dev && kind == o.kind && base == o.base && cols == o.cols && rows == o.rows &&
+        return dev == o.dev && kind == o.kind && f16 == o.f16 && base == o.base && cols == o.cols && rows == o.rows &&
                planes == o.planes && box_rows == o.box_rows;
     }
 };
@@ -71,10 +72,10 @@ CUtensorMap g_maps[kCache];
 int g_used = 0, g_next = 0;
 
 bool cached_map(CUtensorMap* out, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
-                uint32_t box_rows, int kind = 0) {
+                uint32_t box_rows, int kind = 0, bool f16 = false) {
     int dev = 0;
     cudaGetDevice(&dev);
-    MapKey key{dev, kind, base, cols, rows, planes, box_rows};
+    MapKey key{dev, kind, f16 ? 1 : 0, base, cols, rows, planes, box_rows};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         for (int i = 0; i < g_used; ++i)
@@ -84,8 +85,8 @@ bool cached_map(CUtensorMap* out, const void* base, uint64_t cols, uint64_t rows
             }
     }
     CUtensorMap m;
-    const bool ok = kind == 0 ? encode_map_bf16_3d(&m, base, cols, rows, planes, box_rows)
-                              : encode_map_pool_bf16(&m, base, cols, rows, planes, box_rows);
+    const bool ok = kind == 0 ? encode_map_bf16_3d(&m, base, cols, rows, planes, box_rows, f16)
+                              : encode_map_pool_bf16(&m, base, cols, rows, planes, box_rows, f16);
     if (!ok) return false;
     std::lock_guard<std::mutex> lk(g_mu);
     int slot = g_used < kCache ? g_used++ : (g_next++ % kCache);
@@ -108,7 +109,7 @@ int check_common(int B, int Hq, int Hkv, int S, int Sk, int D, float scale, floa
     if (Hq % Hkv != 0) return GBATTN_ERR_INVALID_ARG;
     if (!(std::isfinite(scale) && scale > 0.f)) return GBATTN_ERR_INVALID_ARG;
     if (!(std::isfinite(softcap) && softcap >= 0.f)) return GBATTN_ERR_INVALID_ARG;
-    if (dtype != GBATTN_BF16 && dtype != GBATTN_F32) return GBATTN_ERR_INVALID_ARG;
+    if (dtype != GBATTN_BF16 && dtype != GBATTN_F32 && dtype != GBATTN_F16) return GBATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return GBATTN_ERR_UNSUPPORTED;
     // 32-bit index limits of the kernels' grids and rows.
     if ((long long)B * Hq * S > 0x7fffffffLL || (long long)B * Hkv * Sk > 0x7fffffffLL) return GBATTN_ERR_UNSUPPORTED;
@@ -135,27 +136,29 @@ bool device_facts(unsigned int** status, int* num_sms) {
 }
 
 bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
-                        uint32_t box_rows) {
+                        uint32_t box_rows, bool f16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {cols, rows, planes};
     cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
     cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    const CUtensorMapDataType ty = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return fn(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool encode_map_pool_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t heads, uint64_t rows,
-                          uint32_t box_rows) {
+                          uint32_t box_rows, bool f16) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {cols, heads, rows};
     cuuint64_t strides[2] = {cols * 2, cols * heads * 2};
     cuuint32_t box[3] = {64, 1, box_rows};
     cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    const CUtensorMapDataType ty = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    return fn(map, ty, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -177,7 +180,7 @@ int attn_fwd_ex(const gbattn_fwd_params* a) {
     if (a->row_kv_bounds && (reinterpret_cast<uintptr_t>(a->row_kv_bounds) & 7u)) return GBATTN_ERR_INVALID_ARG;
     if (a->lse_out && (reinterpret_cast<uintptr_t>(a->lse_out) & 3u)) return GBATTN_ERR_INVALID_ARG;
     if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
-    const size_t esz = a->dtype == GBATTN_BF16 ? 2 : 4;
+    const size_t esz = a->dtype == GBATTN_F32 ? 4 : 2;
     const size_t nq = (size_t)a->B * a->Hq * a->Sq * a->D * esz;
     const size_t nkv = (size_t)a->B * a->Hkv * a->Sk * a->D * esz;
     if (overlaps(a->out, nq, a->q, nq) || overlaps(a->out, nq, a->k, nkv) || overlaps(a->out, nq, a->v, nkv))
@@ -203,17 +206,19 @@ int attn_fwd_ex(const gbattn_fwd_params* a) {
     f.wr = a->window_right;
     f.softcap = a->softcap;
     f.timeout_ns = g_timeout_ns;
+    f.f16 = a->dtype == GBATTN_F16;
     if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(a->stream);
     cudaError_t e;
     if (a->dtype == GBATTN_F32) {
         e = launch_prefill_f32(f, st);
     } else {
+        const bool h = f.f16 != 0;
         CUtensorMap tq, tk, tv, to;
-        if (!cached_map(&tq, a->q, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128) ||
-            !cached_map(&tk, a->k, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128) ||
-            !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128) ||
-            !cached_map(&to, a->out, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128))
+        if (!cached_map(&tq, a->q, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h) ||
+            !cached_map(&tk, a->k, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h) ||
+            !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h) ||
+            !cached_map(&to, a->out, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h))
             return GBATTN_ERR_CUDA;
         e = launch_prefill_bf16(f, tq, tk, tv, to, st);
     }
@@ -327,7 +332,7 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
                 void* workspace, size_t workspace_bytes, int dtype, void* stream) {
     int rc = check_common(B, Hq, Hkv, 1, Sk, D, softmax_scale, softcap, dtype);
     if (rc) return rc;
-    if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+    if (dtype == GBATTN_F32) return GBATTN_ERR_UNSUPPORTED;
     if (!q || !k || !v || !out || num_splits < 0) return GBATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GBATTN_ERR_INVALID_ARG;
     if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)) return GBATTN_ERR_INVALID_ARG;
@@ -362,8 +367,10 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
     f.scale = softmax_scale;
     f.softcap = softcap;
     f.timeout_ns = g_timeout_ns;
+    f.f16 = dtype == GBATTN_F16;
     CUtensorMap tk, tv;
-    if (!cached_map(&tk, k, D, Sk, (uint64_t)B * Hkv, 64) || !cached_map(&tv, v, D, Sk, (uint64_t)B * Hkv, 64))
+    if (!cached_map(&tk, k, D, Sk, (uint64_t)B * Hkv, 64, 0, f.f16 != 0) ||
+        !cached_map(&tv, v, D, Sk, (uint64_t)B * Hkv, 64, 0, f.f16 != 0))
         return GBATTN_ERR_CUDA;
     cudaError_t e = launch_decode_bf16(f, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
@@ -394,7 +401,7 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
     if (!paged_geometry(block_size, max_blocks_per_seq, num_blocks, &max_ctx)) return GBATTN_ERR_INVALID_ARG;
     int rc = check_common(B, Hq, Hkv, 1, max_ctx, D, softmax_scale, softcap, dtype);
     if (rc) return rc;
-    if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+    if (dtype == GBATTN_F32) return GBATTN_ERR_UNSUPPORTED;
     if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out || num_splits < 0)
         return GBATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return GBATTN_ERR_INVALID_ARG;
@@ -438,10 +445,12 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
     f.max_blocks = max_blocks_per_seq;
     f.block_size = block_size;
     f.num_blocks = num_blocks;
+    f.f16 = dtype == GBATTN_F16;
     const uint32_t box = block_size < 64 ? (uint32_t)block_size : 64u;
     const uint64_t rows = (uint64_t)num_blocks * block_size;
     CUtensorMap tk, tv;
-    if (!cached_map(&tk, k_cache, D, Hkv, rows, box, 1) || !cached_map(&tv, v_cache, D, Hkv, rows, box, 1))
+    if (!cached_map(&tk, k_cache, D, Hkv, rows, box, 1, f.f16 != 0) ||
+        !cached_map(&tv, v_cache, D, Hkv, rows, box, 1, f.f16 != 0))
         return GBATTN_ERR_CUDA;
     cudaError_t e = launch_decode_bf16(f, tk, tv, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;

@@ -20,6 +20,7 @@
 // lane owns D/32 output dimensions; probabilities reach it through a small
 // per-warp shared buffer.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
@@ -35,8 +36,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
 struct DecParams {
-    const __nv_bfloat16* q;
-    __nv_bfloat16* out;
+    const uint16_t* q;   // bf16 or fp16 bits
+    uint16_t* out;
     float* lse;
     const float* slopes;
     float* ws_o;
@@ -58,6 +59,20 @@ struct DecParams {
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// low / high 16-bit element of a packed pair, bf16 or fp16
+template <bool F16>
+__device__ __forceinline__ float lo16(uint32_t w) {
+    return F16 ? __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))) : bf16lo(w);
+}
+template <bool F16>
+__device__ __forceinline__ float hi16(uint32_t w) {
+    return F16 ? __half2float(__ushort_as_half((unsigned short)(w >> 16))) : bf16hi(w);
+}
+// fp32 -> the 16-bit storage type (round to nearest even), as bits
+template <bool F16>
+__device__ __forceinline__ uint16_t to16(float v) {
+    return F16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
 
 template <int D>
 struct DCfg {
@@ -71,7 +86,7 @@ struct DCfg {
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled slab.
 __device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
-template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED>
+template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED, bool F16>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
     decode_bf16_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                        const DecParams p) {
@@ -193,14 +208,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
 #pragma unroll
     for (int h = 0; h < GC; ++h) {
         const bool hv = h < n_heads;
-        const __nv_bfloat16* qp = p.q + (size_t)(b * p.Hq + h0 + (hv ? h : 0)) * D + dq * DQ;
+        const uint16_t* qp = p.q + (size_t)(b * p.Hq + h0 + (hv ? h : 0)) * D + dq * DQ;
 #pragma unroll
         for (int d = 0; d < DQ; d += 8) {
             const uint4 w = hv ? *reinterpret_cast<const uint4*>(qp + d) : make_uint4(0, 0, 0, 0);
-            q2[h][d / 2 + 0] = make_float2(bf16lo(w.x) * p.qscale, bf16hi(w.x) * p.qscale);
-            q2[h][d / 2 + 1] = make_float2(bf16lo(w.y) * p.qscale, bf16hi(w.y) * p.qscale);
-            q2[h][d / 2 + 2] = make_float2(bf16lo(w.z) * p.qscale, bf16hi(w.z) * p.qscale);
-            q2[h][d / 2 + 3] = make_float2(bf16lo(w.w) * p.qscale, bf16hi(w.w) * p.qscale);
+            q2[h][d / 2 + 0] = make_float2(lo16<F16>(w.x) * p.qscale, hi16<F16>(w.x) * p.qscale);
+            q2[h][d / 2 + 1] = make_float2(lo16<F16>(w.y) * p.qscale, hi16<F16>(w.y) * p.qscale);
+            q2[h][d / 2 + 2] = make_float2(lo16<F16>(w.z) * p.qscale, hi16<F16>(w.z) * p.qscale);
+            q2[h][d / 2 + 3] = make_float2(lo16<F16>(w.w) * p.qscale, hi16<F16>(w.w) * p.qscale);
         }
     }
     const float slope_l2 = (ALIBI && hsel < n_heads) ? p.slopes[h0 + hsel] * LOG2E : 0.f;
@@ -237,8 +252,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
                 const int dim = dq * DQ + c8 * 8;
                 const int slab = dim >> 6, chunk = (dim & 63) >> 3;
                 const uint4 w = *reinterpret_cast<const uint4*>(ks + slab * C::SLAB + swz(r, chunk));
-                const float2 k2[4] = {make_float2(bf16lo(w.x), bf16hi(w.x)), make_float2(bf16lo(w.y), bf16hi(w.y)),
-                                      make_float2(bf16lo(w.z), bf16hi(w.z)), make_float2(bf16lo(w.w), bf16hi(w.w))};
+                const float2 k2[4] = {make_float2(lo16<F16>(w.x), hi16<F16>(w.x)),
+                                      make_float2(lo16<F16>(w.y), hi16<F16>(w.y)),
+                                      make_float2(lo16<F16>(w.z), hi16<F16>(w.z)),
+                                      make_float2(lo16<F16>(w.w), hi16<F16>(w.w))};
 #pragma unroll
                 for (int h = 0; h < GC; ++h)
 #pragma unroll
@@ -321,11 +338,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
                 float2 v2[DV / 2];
                 if (DV == 4) {
                     const uint2 w = *reinterpret_cast<const uint2*>(vp);
-                    v2[0] = make_float2(bf16lo(w.x), bf16hi(w.x));
-                    v2[DV / 2 - 1] = make_float2(bf16lo(w.y), bf16hi(w.y));
+                    v2[0] = make_float2(lo16<F16>(w.x), hi16<F16>(w.x));
+                    v2[DV / 2 - 1] = make_float2(lo16<F16>(w.y), hi16<F16>(w.y));
                 } else {
                     const uint32_t w = *reinterpret_cast<const uint32_t*>(vp);
-                    v2[0] = make_float2(bf16lo(w), bf16hi(w));
+                    v2[0] = make_float2(lo16<F16>(w), hi16<F16>(w));
                 }
 #pragma unroll
                 for (int h = 0; h < GC; ++h) {
@@ -374,7 +391,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         const int head = h0 + h;
         const size_t row = (size_t)b * p.Hq + head;
         if (p.num_splits == 1) {
-            p.out[row * D + d] = __float2bfloat16_rn(val);
+            p.out[row * D + d] = to16<F16>(val);
             if (p.lse && d == 0) p.lse[row] = lse2 * LN2;
         } else {
             const size_t prow = row * p.num_splits + split;
@@ -385,10 +402,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
 }
 
 // Combine: one block per (b, h) row, one thread per output dimension.
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ ws_o,
                                                            const float* __restrict__ ws_lse,
-                                                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                           uint16_t* __restrict__ out, float* __restrict__ lse,
                                                            int num_splits, float lse_to_natural) {
     const size_t row = blockIdx.x;
     const int d = threadIdx.x;
@@ -403,13 +420,13 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
             O += w * ws_o[(row * num_splits + s) * D + d];
         }
     }
-    out[row * D + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    out[row * D + d] = to16<F16>(L > 0.f ? O / L : 0.f);
     if (lse && d == 0) lse[row] = (L > 0.f) ? (M + log2f(L)) * lse_to_natural : -INFINITY;
 }
 
-template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED>
+template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED, bool F16>
 cudaError_t launch_dec(const DecParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
-    auto kern = decode_bf16_kernel<D, GC, SOFTCAP, ALIBI, PAGED>;
+    auto kern = decode_bf16_kernel<D, GC, SOFTCAP, ALIBI, PAGED, F16>;
     const int smem = DCfg<D>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -418,25 +435,28 @@ cudaError_t launch_dec(const DecParams& p, const CUtensorMap& tk, const CUtensor
     e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1) return e;
     // every partial lse is in base 2 (logits carry the log2(e) factor).
-    decode_combine_kernel<D><<<p.B * p.Hq, D, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits, LN2);
+    decode_combine_kernel<D, F16><<<p.B * p.Hq, D, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits, LN2);
     return cudaGetLastError();
 }
 
-template <int D, int GC, bool PAGED>
+template <int D, int GC, bool PAGED, bool F16>
 cudaError_t launch_dec_caps(const DecParams& p, bool cap, bool ali, const CUtensorMap& tk, const CUtensorMap& tv,
                             cudaStream_t s) {
     if (cap)
-        return ali ? launch_dec<D, GC, true, true, PAGED>(p, tk, tv, s)
-                   : launch_dec<D, GC, true, false, PAGED>(p, tk, tv, s);
-    return ali ? launch_dec<D, GC, false, true, PAGED>(p, tk, tv, s)
-               : launch_dec<D, GC, false, false, PAGED>(p, tk, tv, s);
+        return ali ? launch_dec<D, GC, true, true, PAGED, F16>(p, tk, tv, s)
+                   : launch_dec<D, GC, true, false, PAGED, F16>(p, tk, tv, s);
+    return ali ? launch_dec<D, GC, false, true, PAGED, F16>(p, tk, tv, s)
+               : launch_dec<D, GC, false, false, PAGED, F16>(p, tk, tv, s);
 }
 
 template <int D, int GC>
-cudaError_t launch_dec_flags(const DecParams& p, bool cap, bool ali, bool paged, const CUtensorMap& tk,
+cudaError_t launch_dec_flags(const DecParams& p, bool cap, bool ali, bool paged, bool f16, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t s) {
-    return paged ? launch_dec_caps<D, GC, true>(p, cap, ali, tk, tv, s)
-                 : launch_dec_caps<D, GC, false>(p, cap, ali, tk, tv, s);
+    if (f16)
+        return paged ? launch_dec_caps<D, GC, true, true>(p, cap, ali, tk, tv, s)
+                     : launch_dec_caps<D, GC, false, true>(p, cap, ali, tk, tv, s);
+    return paged ? launch_dec_caps<D, GC, true, false>(p, cap, ali, tk, tv, s)
+                 : launch_dec_caps<D, GC, false, false>(p, cap, ali, tk, tv, s);
 }
 
 }  // namespace
@@ -471,8 +491,8 @@ void decode_split_plan(int B, int Hkv, int Sk, int num_sms, int requested, int* 
 cudaError_t launch_decode_bf16(const DecodeProblem& f, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream) {
     DecParams p{};
-    p.q = static_cast<const __nv_bfloat16*>(f.q);
-    p.out = static_cast<__nv_bfloat16*>(f.out);
+    p.q = static_cast<const uint16_t*>(f.q);
+    p.out = static_cast<uint16_t*>(f.out);
     p.lse = f.lse;
     p.slopes = f.slopes;
     p.ws_o = f.ws_o;
@@ -504,16 +524,16 @@ cudaError_t launch_decode_bf16(const DecodeProblem& f, const CUtensorMap& tk, co
     if (f.D == 128) {
         const int GC = G >= 4 ? 4 : (G == 3 ? 4 : (G == 2 ? 2 : 1));
         p.n_chunks = (G + GC - 1) / GC;
-        if (GC == 4) return launch_dec_flags<128, 4>(p, cap, ali, paged, tk, tv, stream);
-        if (GC == 2) return launch_dec_flags<128, 2>(p, cap, ali, paged, tk, tv, stream);
-        return launch_dec_flags<128, 1>(p, cap, ali, paged, tk, tv, stream);
+        if (GC == 4) return launch_dec_flags<128, 4>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
+        if (GC == 2) return launch_dec_flags<128, 2>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
+        return launch_dec_flags<128, 1>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
     }
     const int GC = G >= 5 ? 8 : (G >= 3 ? 4 : (G == 2 ? 2 : 1));
     p.n_chunks = (G + GC - 1) / GC;
-    if (GC == 8) return launch_dec_flags<64, 8>(p, cap, ali, paged, tk, tv, stream);
-    if (GC == 4) return launch_dec_flags<64, 4>(p, cap, ali, paged, tk, tv, stream);
-    if (GC == 2) return launch_dec_flags<64, 2>(p, cap, ali, paged, tk, tv, stream);
-    return launch_dec_flags<64, 1>(p, cap, ali, paged, tk, tv, stream);
+    if (GC == 8) return launch_dec_flags<64, 8>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
+    if (GC == 4) return launch_dec_flags<64, 4>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
+    if (GC == 2) return launch_dec_flags<64, 2>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
+    return launch_dec_flags<64, 1>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
 }
 
 }  // namespace gbattn

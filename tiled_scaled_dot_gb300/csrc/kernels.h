@@ -27,6 +27,7 @@ struct FwdProblem {
     int num_sms;
     // packed variable-length sequences (q / out [total_q, Hq, D], k / v
     // [total_k, Hkv, D]); Sq is then the longest sequence's query count
+    int f16;                    // 16-bit inputs are fp16 (else bf16)
     int varlen;
     const int* cu_q;            // [B + 1]
     const int* cu_k;            // [B + 1]
@@ -53,6 +54,7 @@ struct DecodeProblem {
     int num_sms;
     // paged cache (k, v are pools [num_blocks, block_size, Hkv, D]); Sk is the
     // longest context the block table can hold (max_blocks * block_size)
+    int f16;                       // fp16 inputs / output (else bf16)
     int paged;
     const uint32_t* block_table;   // [B, max_blocks]
     const uint32_t* context_lens;  // [B]
@@ -72,16 +74,17 @@ enum : unsigned int {
     ST_DIAG = 1u << 16,
 };
 
-// 3-D bf16 tensor map over a contiguous [planes][rows][cols] array with
-// a {64, box_rows, 1} box and 128-byte swizzle; out-of-range rows read as 0.
+// 3-D 16-bit (bf16, or fp16 when f16) tensor map over a contiguous
+// [planes][rows][cols] array with a {64, box_rows, 1} box and 128-byte
+// swizzle; out-of-range rows read as 0.
 bool encode_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t planes,
-                        uint32_t box_rows);
+                        uint32_t box_rows, bool f16 = false);
 
 // 3-D bf16 tensor map over a paged pool [rows][heads][cols] (rows = num_blocks *
 // block_size tokens) with a {64, 1, box_rows} box and 128-byte swizzle: one
 // box is box_rows consecutive tokens of one head; rows past the pool read as 0.
 bool encode_map_pool_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t heads, uint64_t rows,
-                          uint32_t box_rows);
+                          uint32_t box_rows, bool f16 = false);
 
 // Kernel launchers.  Each returns the launch's cudaError_t.
 cudaError_t launch_prefill_bf16(const FwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tk,

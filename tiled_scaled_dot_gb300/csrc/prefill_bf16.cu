@@ -94,7 +94,7 @@ struct Cfg {
 };
 
 struct Params {
-    __nv_bfloat16* out;
+    uint16_t* out;     // bf16 or fp16 bits
     float* lse;
     const float* slopes;
     const int2* rowb;
@@ -279,7 +279,7 @@ __device__ __forceinline__ int read_item(Smem& sm, int k, const WaitCtl& wc, uin
 }
 
 // ---------------------------------------------------------------------------- softmax role
-template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN>
+template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN, bool F16>
 __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t tmem, const WaitCtl& wc,
                                              int warp) {
     using C = Cfg<D>;
@@ -377,7 +377,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
                 y = (SOFTCAP || ALIBI) ? __fadd2_rn(y, nm) : __ffma2_rn(y, sl2, nm);
                 const float2 pp = make_float2(ex2_approx(y.x), ex2_approx(y.y));
                 acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], pp);
-                pw[j >> 1] = pack_bf16x2(pp.x, pp.y);
+                pw[j >> 1] = pack16x2<F16>(pp.x, pp.y);
             }
             const float2 a01 = __fadd2_rn(acc[0], acc[1]), a23 = __fadd2_rn(acc[2], acc[3]);
             const float2 a = __fadd2_rn(a01, a23);
@@ -412,7 +412,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
 }
 
 // ---------------------------------------------------------------------------- epilogue role
-template <int D, bool VARLEN>
+template <int D, bool VARLEN, bool F16>
 __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_t tmem, const WaitCtl& wc,
                                               int warp, uint8_t* stage, const CUtensorMap* tmO) {
     // Output rows go through a 128-row x 64-column bf16 staging tile in shared
@@ -484,10 +484,10 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
                     for (int i = 0; i < 4; ++i) {
                         const int c = c32 * 4 + i;  // 16-byte chunk of the 128-byte staging row
                         uint4 w;
-                        w.x = pack_bf16x2(ov[8 * i + 0] * inv_l, ov[8 * i + 1] * inv_l);
-                        w.y = pack_bf16x2(ov[8 * i + 2] * inv_l, ov[8 * i + 3] * inv_l);
-                        w.z = pack_bf16x2(ov[8 * i + 4] * inv_l, ov[8 * i + 5] * inv_l);
-                        w.w = pack_bf16x2(ov[8 * i + 6] * inv_l, ov[8 * i + 7] * inv_l);
+                        w.x = pack16x2<F16>(ov[8 * i + 0] * inv_l, ov[8 * i + 1] * inv_l);
+                        w.y = pack16x2<F16>(ov[8 * i + 2] * inv_l, ov[8 * i + 3] * inv_l);
+                        w.z = pack16x2<F16>(ov[8 * i + 4] * inv_l, ov[8 * i + 5] * inv_l);
+                        w.w = pack16x2<F16>(ov[8 * i + 6] * inv_l, ov[8 * i + 7] * inv_l);
                         if (ragged) {
                             if (live) reinterpret_cast<uint4*>(p.out + orow * D + hf * 64)[c] = w;
                         } else {
@@ -513,7 +513,7 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
     if (issuer) bulk_wait_group0();
 }
 
-template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN>
+template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN, bool F16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -567,10 +567,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Each warpgroup executes one setmaxnreg, at one program point, before its roles split.
     if (warp < 8) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::SOFTMAX_REGS));
-        softmax_role<D, SOFTCAP, ALIBI, VARLEN>(p, sm, tmem, wc, warp);
+        softmax_role<D, SOFTCAP, ALIBI, VARLEN, F16>(p, sm, tmem, wc, warp);
     } else if (warp < 12) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::EPI_REGS));
-        epilogue_role<D, VARLEN>(p, sm, tmem, wc, warp, sStage, &tmO);
+        epilogue_role<D, VARLEN, F16>(p, sm, tmem, wc, warp, sStage, &tmO);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::CONTROL_REGS));
         if (warp == WARP_PRODUCER) {
@@ -702,8 +702,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, ST_PREFILL_MMA));
             };
-            constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, 0);
-            constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, 1);
+            constexpr uint32_t IDESC_S = F16 ? idesc_f16_f32(BM, BN, 0) : idesc_bf16_f32(BM, BN, 0);
+            constexpr uint32_t IDESC_O = F16 ? idesc_f16_f32(BM, D, 1) : idesc_bf16_f32(BM, D, 1);
             uint32_t ld_cnt = 0, grp_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
             bool ok = true;
             const uint32_t sQa[2] = {smem_u32(sQ[0]), smem_u32(sQ[1])};
@@ -814,10 +814,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
 }
 
-template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN>
+template <int D, bool SOFTCAP, bool ALIBI, bool VARLEN, bool F16>
 cudaError_t launch_variant(const Params& prm, int grid, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
-    auto kern = prefill_bf16_kernel<D, SOFTCAP, ALIBI, VARLEN>;
+    auto kern = prefill_bf16_kernel<D, SOFTCAP, ALIBI, VARLEN, F16>;
     const int smem = Cfg<D>::SMEM_BYTES;
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -831,19 +831,19 @@ cudaError_t launch_variant(const Params& prm, int grid, const CUtensorMap& tq, c
     return cudaGetLastError();
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool F16>
 cudaError_t launch_flags(const Params& p, int grid, int D, bool cap, bool ali, const CUtensorMap& tq,
                          const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
     if (D == 128) {
-        if (cap) return ali ? launch_variant<128, true, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
-                            : launch_variant<128, true, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
-        return ali ? launch_variant<128, false, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
-                   : launch_variant<128, false, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
+        if (cap) return ali ? launch_variant<128, true, true, VARLEN, F16>(p, grid, tq, tk, tv, to, stream)
+                            : launch_variant<128, true, false, VARLEN, F16>(p, grid, tq, tk, tv, to, stream);
+        return ali ? launch_variant<128, false, true, VARLEN, F16>(p, grid, tq, tk, tv, to, stream)
+                   : launch_variant<128, false, false, VARLEN, F16>(p, grid, tq, tk, tv, to, stream);
     }
-    if (cap) return ali ? launch_variant<64, true, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
-                        : launch_variant<64, true, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
-    return ali ? launch_variant<64, false, true, VARLEN>(p, grid, tq, tk, tv, to, stream)
-               : launch_variant<64, false, false, VARLEN>(p, grid, tq, tk, tv, to, stream);
+    if (cap) return ali ? launch_variant<64, true, true, VARLEN, F16>(p, grid, tq, tk, tv, to, stream)
+                        : launch_variant<64, true, false, VARLEN, F16>(p, grid, tq, tk, tv, to, stream);
+    return ali ? launch_variant<64, false, true, VARLEN, F16>(p, grid, tq, tk, tv, to, stream)
+               : launch_variant<64, false, false, VARLEN, F16>(p, grid, tq, tk, tv, to, stream);
 }
 
 }  // namespace
@@ -851,7 +851,7 @@ cudaError_t launch_flags(const Params& p, int grid, int D, bool cap, bool ali, c
 cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
     Params p{};
-    p.out = static_cast<__nv_bfloat16*>(f.out);
+    p.out = static_cast<uint16_t*>(f.out);
     p.lse = f.lse;
     p.slopes = f.slopes;
     p.rowb = reinterpret_cast<const int2*>(f.row_bounds);
@@ -883,8 +883,10 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
         p.n_items = ((p.n_qt + 1) / 2) * f.B * f.Hq;
     const int grid = p.n_items < f.num_sms ? p.n_items : f.num_sms;
     const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
-    return p.varlen ? launch_flags<true>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream)
-                    : launch_flags<false>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream);
+    // packed sequences are built for bf16 only
+    if (p.varlen) return launch_flags<true, false>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream);
+    return f.f16 ? launch_flags<false, true>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream)
+                 : launch_flags<false, false>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream);
 }
 
 }  // namespace gbattn

@@ -180,6 +180,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn) {
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// The same with fp16 operands (A and B formats 0): kind::f16 takes both
+// operands in one type, bf16 or fp16.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, int b_mn) {
+    return (1u << 4)                                   // D format: f32
+           | (static_cast<uint32_t>(b_mn & 1) << 16)   // B major
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.  The tile is made of
 // 8-row x 128-byte atoms (1024 bytes, 1024-byte aligned).
 //   K-major:  rows are M/N indices, 128 bytes = 64 bf16 of K per row;
@@ -379,6 +388,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// fp16x2 pack, round to nearest even: `lo` goes to the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// The pair in the 16-bit storage type of a path (bf16 or fp16).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16x2(float lo, float hi) {
+    return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
