@@ -169,9 +169,11 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "2a5caa08642b62e7"): 128801792,
-    # decode: full-size one-pass capture, printed to three significant figures
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "618bfb227641ba53"): 2169430000,
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "44448ea791b58e8c"): 128985600,
+    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "44448ea791b58e8c"): 4025290000,
+    # decode: full-size one-pass captures, printed to three or four significant figures
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "72cd91cd0687498b"): 2169030000,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "72cd91cd0687498b"): 1759100000,
 }
 
 
