@@ -161,28 +161,42 @@ def max_over_ranks(x: float, ws: int) -> float:
 # ----------------------------------------------------------------------------- ncu traffic
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
 # dominant kernel, from one ncu capture, keyed by a fingerprint of the
-# kernel's source files: a changed kernel reports null until it is captured
-# again.  The captures and their commands are summarised under profiles/.
+# kernel's source files (comments and whitespace excluded): a changed kernel
+# reports null until it is captured again.  The captures and their commands
+# are summarised under profiles/.
 KERNEL_SOURCES = {
     "prefill": ("prefill_bf16.cu", "ptx.cuh", "kernels.h"),
     "decode": ("decode_bf16.cu", "ptx.cuh", "kernels.h"),
 }
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "44448ea791b58e8c"): 128985600,
-    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "44448ea791b58e8c"): 4025290000,
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "96829f447537020b"): 128985600,
+    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "96829f447537020b"): 4025290000,
     # decode: full-size one-pass captures, printed to three or four significant figures
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "72cd91cd0687498b"): 2169030000,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "72cd91cd0687498b"): 1759100000,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "50e267c36253ffd9"): 2169030000,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "50e267c36253ffd9"): 1759100000,
 }
 
 
-def kernel_fingerprint(kind):
+def source_tokens(text):
+    """C/C++ source without comments and whitespace: what the compiler sees
+    of it, so that an edit to a comment keeps a kernel's fingerprint."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return "".join(text.split())
+
+
+def kernel_fingerprint(kind, read=None):
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "tiled_scaled_dot_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(ROOT, "tiled_scaled_dot_gb300", "csrc", f)) as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(source_tokens(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -19,6 +19,10 @@
 // head with packed FFMA2 and a shuffle reduce-scatter sums the groups.  P V:
 // lane owns D/32 output dimensions; probabilities reach it through a small
 // per-warp shared buffer.
+//
+// Template flags: PAGED reads K and V through a block table from a pool
+// [num_blocks, block_size, Hkv, D] (attention.fkc.md, "attention_paged_naive"),
+// with per-sequence context lengths; F16 reads and writes fp16 instead of bf16.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 

@@ -1,4 +1,6 @@
-// prefill_bf16.cu -- bf16 attention forward on tcgen05 tensor cores (sm_103a).
+// prefill_bf16.cu -- 16-bit (bf16, or fp16 with the F16 flag) attention
+// forward on tcgen05 tensor cores (sm_103a), dense [B, H, S, D] problems or
+// packed variable-length sequences (the VARLEN flag).
 //
 // Computes the tiled online-softmax recurrence of "gfx942 unified attention,
 // from the math up", section 3 (running max m, denominator l, rescale
@@ -10,12 +12,15 @@
 //   WG0 (warps 0-3)    softmax for query slot 0: thread r owns query row r,
 //                      which is TMEM lane r of the slot's S and O tiles
 //   WG1 (warps 4-7)    softmax for query slot 1
-//   WG2 (warps 8-11)   epilogue for both slots: O / l -> bf16 rows, lse
-//   WG3 warp 12        TMA producer: Q tiles once per item, K/V tiles through
-//                      an NS-stage shared-memory ring (128-byte swizzle)
-//   WG3 warp 13        MMA issuer (one thread): S = Q K^T with both operands in
-//                      shared memory, O += P V with P in TMEM and V in shared
-//                      memory, fp32 accumulators in TMEM
+//   WG2 (warps 8-11)   epilogue for both slots: O / l -> 16-bit rows, lse
+//   WG3 warp 12        TMA producer: decodes each work item once and publishes
+//                      it to the other roles, loads Q tiles once per item and
+//                      K/V tiles through an NS-stage shared-memory ring
+//                      (128-byte swizzle)
+//   WG3 warp 13        MMA issuer (the whole warp runs the loop, one elected
+//                      lane issues): S = Q K^T with both operands in shared
+//                      memory, O += P V with P in TMEM and V in shared memory,
+//                      fp32 accumulators in TMEM
 //   WG3 warps 14-15    idle
 // Registers move to the softmax warpgroups with setmaxnreg:
 // 2 x 128 x SOFTMAX_REGS + 128 x (EPI_REGS + CONTROL_REGS) <= 512 x LAUNCH_REGS,
@@ -29,7 +34,7 @@
 // boustrophedon order, so causal work evens out across SMs.
 //
 // TMEM columns (512 allocated): S/P of slot x at 128 x, O of slot x at
-// 256 + D x.  P (bf16, two per 32-bit column) overwrites the first 64 columns of
+// 256 + D x.  P (16-bit, two per 32-bit column) overwrites the first 64 columns of
 // its S tile; the next Q K^T into that tile is issued after the P V that reads
 // it, and tcgen05 operations issued by one thread execute in order.
 //
@@ -58,7 +63,8 @@ constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // base-2 units
 constexpr int LAUNCH_REGS = 128;          // 65536 / 512
 // K/V tiles move through the shared-memory slots in the order the MMA thread
-// reads them: per item K_lo, then (V_u, K_{u+1}) for each tile u, V_hi last.
+// reads them, last key tile first: per item K_hi, then (V_u, K_{u-1}) for each
+// tile u > lo, V_lo last.
 // Each of these groups is one MMA step and has one full barrier (the TMA
 // transaction count of its one or two tiles) and one empty barrier (one
 // commit after the step's MMAs), so a step costs the MMA thread one wait and
