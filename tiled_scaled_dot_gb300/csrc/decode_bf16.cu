@@ -471,16 +471,24 @@ void decode_split_plan(int B, int Hkv, int Sk, int num_sms, int requested, int* 
     if (requested > 0) {
         s_best = requested < tiles ? requested : tiles;
     } else {
-        // Pick the split count whose waves of resident CTAs waste the least
-        // time: minimise ceil(rows * s / slots) * ceil(tiles / s).
+        // Time of a split count s, in tiles streamed by one CTA: waves of
+        // resident CTAs (2 per SM) times (tiles per split + a fixed cost of about
+        // three tiles per CTA: loading q, merging the warps, writing the partial,
+        // and its share of the combine), as measured on GB300 decode shapes.
+        // With fewer than about three waves of CTAs in flight the per-CTA
+        // streaming rate, not HBM, bounds the decode, so s starts there.
         const long long rows = (long long)B * Hkv;
         const long long slots = (long long)(num_sms > 0 ? num_sms : 1) * 2;
+        const int s_cap = tiles < 256 ? tiles : 256;
+        long long s_min = (3 * slots + rows - 1) / rows;
+        if (s_min > s_cap) s_min = s_cap;
+        if (s_min < 1) s_min = 1;
         long long best = -1;
-        for (int s = 1; s <= tiles && s <= 256; ++s) {
+        for (int s = (int)s_min; s <= s_cap; ++s) {
             const int ct = (tiles + s - 1) / s;
             if ((tiles + ct - 1) / ct != s) continue;  // same chunking as a smaller s
             const long long waves = (rows * s + slots - 1) / slots;
-            const long long cost = waves * ct * 64 + s;  // small bias towards fewer splits
+            const long long cost = waves * (ct + 3);
             if (best < 0 || cost < best) {
                 best = cost;
                 s_best = s;
