@@ -173,8 +173,8 @@ NCU_TRAFFIC = {
     ("prefill", "bf16_causal_b4_h32_s2048_d128", "96829f447537020b"): 128985600,
     ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "96829f447537020b"): 4025290000,
     # decode: full-size one-pass captures, printed to three or four significant figures
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "50e267c36253ffd9"): 2169030000,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "50e267c36253ffd9"): 1759100000,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "2e9e7234d6afbf6e"): 2157160000,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "2e9e7234d6afbf6e"): 1747050000,
 }
 
 
