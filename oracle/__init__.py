@@ -23,9 +23,14 @@ with a cu_seqlens_q prefix sum, seqused_k per sequence) with the causal mask
 aligned bottom-right (section 4): query i of a sequence sits at absolute
 position kv_len - q_len + i.
 
+``attn_bwd`` is the backward by recompute (attention.fkc.md,
+"attention_flash_backward"): dQ, dK, dV of the forward above, with the softcap
+derivative, dK / dV summed over each GQA group.
+
 Parity pins: every function here is pinned by tests/test_oracle_pins.py,
-tests/test_oracle_varlen.py and tests/test_oracle_paged.py (closed forms, brute force, library special cases,
-invariants); none is "parity unpinned".
+tests/test_oracle_varlen.py, tests/test_oracle_paged.py and
+tests/test_oracle_bwd.py (closed forms, brute force, library special cases,
+invariants, finite differences of the forward); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -313,3 +318,74 @@ def attn_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, seqused_k=None, scale=No
                 out[cq[b] + i, h] = (w @ vb[:, g, :]) / L
                 lse[h, cq[b] + i] = m + torch.log(L)
     return (out, lse) if return_lse else out
+
+
+def attn_bwd(q, k, v, dout, *, scale=None, causal=False, window_left=None, window_right=None,
+             softcap=None, alibi_slopes=None, row_kv_bounds=None):
+    """Attention backward by recompute, in float64 (attention.fkc.md,
+    "attention_flash_backward").
+
+    q, dout [B, Hq, Sq, D]; k, v [B, Hkv, Sk, D]; the forward's flags as in
+    ``attn``.  For each (b, h) the forward is recomputed: the pre-softcap score
+    s_pre = scale q.k, the score s = c tanh(s_pre / c) (softcap) + slope_h (j - i)
+    (ALiBi), -inf where key j is not admissible for row i, and the stable
+    softmax P of each row.  Then, in the contract's order:
+      dV[j]  += sum_i P[i, j] dO[i]
+      dP[i, j] = dO[i] . V[j]
+      dS[i, j] = (dP[i, j] - sum_j' P[i, j'] dP[i, j']) P[i, j],
+                 times 1 - tanh^2(s_pre / c) when softcap is set
+      dQ[i]  += scale sum_j dS[i, j] K[j]
+      dK[j]  += scale sum_i dS[i, j] Q[i]
+    dK and dV of kv head g sum the contributions of every query head of its
+    group; a row with no admissible key contributes nothing.  Returns float64
+    (dq [B, Hq, Sq, D], dk [B, Hkv, Sk, D], dv [B, Hkv, Sk, D]).
+    """
+    q, k, v, s_, rb, (B, Hq, Hkv, Sq, Sk, D) = _prep(q, k, v, alibi_slopes, row_kv_bounds)
+    if dout.shape != q.shape:
+        raise ValueError("dout must have q's shape")
+    do = dout.detach().to("cpu", torch.float64)
+    q, k, v = q.double(), k.double(), v.double()
+    G = Hq // Hkv
+    sc = _f32(1.0 / (D ** 0.5) if scale is None else scale)
+    cap = 0.0 if not softcap else _f32(softcap)
+    slopes = None if s_ is None else s_.double()
+    wl, wr = _win(window_left), _win(window_right)
+    i = torch.arange(Sq, dtype=torch.int64)[:, None]
+    j = torch.arange(Sk, dtype=torch.int64)[None, :]
+    adm0 = torch.ones(Sq, Sk, dtype=torch.bool)
+    if causal:
+        adm0 &= j <= i
+    if wl >= 0:
+        adm0 &= j + wl >= i
+    if wr >= 0:
+        adm0 &= j <= i + wr
+    dq = torch.zeros(B, Hq, Sq, D, dtype=torch.float64)
+    dk = torch.zeros(B, Hkv, Sk, D, dtype=torch.float64)
+    dv = torch.zeros(B, Hkv, Sk, D, dtype=torch.float64)
+    for b in range(B):
+        adm = adm0.clone()
+        if rb is not None:
+            lo = rb[b, :, 0].long()[:, None]
+            hi = rb[b, :, 1].long()[:, None]
+            adm &= (j >= lo) & (j <= hi)
+        live = adm.any(dim=1)  # rows with at least one admissible key
+        for h in range(Hq):
+            g = h // G
+            s_pre = sc * (q[b, h] @ k[b, g].T)  # [Sq, Sk]
+            s = cap * torch.tanh(s_pre / cap) if cap else s_pre.clone()
+            if slopes is not None:
+                s = s + slopes[h] * (j - i).double()
+            s = torch.where(adm, s, torch.full_like(s, float("-inf")))
+            m = torch.where(live, s.max(dim=1).values, torch.zeros(Sq, dtype=torch.float64))
+            w = torch.where(adm, torch.exp(s - m[:, None]), torch.zeros_like(s))
+            L = w.sum(dim=1)
+            P = torch.where(live[:, None], w / torch.where(live, L, torch.ones_like(L))[:, None],
+                            torch.zeros_like(w))
+            dv[b, g] += P.T @ do[b, h]
+            dP = do[b, h] @ v[b, g].T
+            dS = (dP - (P * dP).sum(dim=1, keepdim=True)) * P
+            if cap:
+                dS = dS * (1.0 - torch.tanh(s_pre / cap) ** 2)
+            dq[b, h] = sc * (dS @ k[b, g])
+            dk[b, g] += sc * (dS.T @ q[b, h])
+    return dq, dk, dv
