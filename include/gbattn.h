@@ -245,6 +245,65 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
                       float softmax_scale, float softcap, int num_splits, void* workspace, size_t workspace_bytes,
                       int dtype, void* stream);
 
+/*
+ * attn_bwd -- attention backward by recompute (attention.fkc.md,
+ * "attention_flash_backward"): given dO, the gradients of the forward above
+ * (same flags, same causal / window / row-bound mask, same softcap and ALiBi),
+ *
+ *     P      = the forward's softmax, recomputed per row from q, k and lse
+ *     dV_j   = sum_i P_ij dO_i                       (summed over the GQA group)
+ *     dS_ij  = P_ij (dO_i . V_j - dO_i . O_i)        times 1 - tanh^2(s_pre / c)
+ *                                                    with softcap c, s_pre the
+ *                                                    scaled score before capping
+ *     dQ_i   = softmax_scale sum_j dS_ij K_j
+ *     dK_j   = softmax_scale sum_i dS_ij Q_i         (summed over the GQA group)
+ *
+ * A row with no admissible key contributes nothing (its dQ row is zero).  The
+ * result is deterministic: no atomics, a fixed summation order.
+ *
+ *  q, k, v, dout   device, [B, Hq, Sq, D], [B, Hkv, Sk, D] x 2, [B, Hq, Sq, D].
+ *  out, lse        the forward's output [B, Hq, Sq, D] and lse [B, Hq, Sq]
+ *                  (attn_fwd_ex with lse_out), both given or both NULL; when
+ *                  NULL the forward is recomputed into the workspace first.
+ *  alibi_slopes, row_kv_bounds, softmax_scale, causal, window_left,
+ *  window_right, softcap   as in attn_fwd_ex.
+ *  dq              device [B, Hq, Sq, D], written fully.
+ *  dk, dv          device [B, Hkv, Sk, D], written fully.
+ *  dtype           GBATTN_BF16 or GBATTN_F16 for every 16-bit tensor
+ *                  (GBATTN_F32 returns GBATTN_ERR_UNSUPPORTED); D 64 or 128.
+ *  workspace       device, 256-byte aligned, at least
+ *                  attn_bwd_workspace_size(...) bytes (recompute = 1 when out
+ *                  and lse are NULL); the caller owns it; its contents are
+ *                  scratch.
+ *  Errors: GBATTN_ERR_INVALID_ARG also for a gradient buffer that overlaps an
+ *  input, another gradient or the workspace.
+ */
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* out;
+    const float* lse;
+    const void* dout;
+    const float* alibi_slopes;
+    const int32_t* row_kv_bounds;
+    void* dq;
+    void* dk;
+    void* dv;
+    int B, Hq, Hkv, Sq, Sk, D;
+    float softmax_scale;
+    int causal;
+    int window_left, window_right;
+    float softcap;
+    int dtype;
+    void* workspace;
+    size_t workspace_bytes;
+    void* stream;
+} gbattn_bwd_params;
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int recompute);
+int attn_bwd(const gbattn_bwd_params* p);
+
 /* Human-readable text of a status code (static storage). */
 const char* gbattn_status_string(int status);
 

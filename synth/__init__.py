@@ -37,6 +37,7 @@ STREAM_Q = 0
 STREAM_K = 1
 STREAM_V = 2
 STREAM_AUX = 3
+STREAM_DO = 5  # upstream gradient dO of the backward (4 is the paged pool's block shuffle)
 
 
 def _s64(x: int) -> int:

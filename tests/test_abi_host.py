@@ -156,3 +156,39 @@ def test_varlen_rejects_bad_arguments(L):
     assert call(21, 1) == 2           # fp32 not built
     assert call(21, 2) == 2           # fp16 varlen not built
     assert call(7, P(FAKE)) == 1      # out aliasing q
+
+
+def test_backward_rejects_bad_arguments(L):
+    import tiled_scaled_dot_gb300 as g
+    L.attn_bwd.argtypes = [ctypes.POINTER(g._BwdParams)]
+    B, Hq, Hkv, S, D = 2, 4, 2, 256, 128
+    ws_need = L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 1)
+    ws_given = L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 0)
+    assert ws_need > ws_given > 0
+    assert L.attn_bwd_workspace_size(B, 3, Hkv, S, S, D, 1) == 0  # Hq % Hkv
+    nq, nkv = B * Hq * S * D * 2, B * Hkv * S * D * 2
+    base = dict(q=FAKE, k=FAKE + nq, v=FAKE + nq + nkv, dout=FAKE + 2 * nq + 2 * nkv, dq=FAKE * 64,
+                dk=FAKE * 64 + nq, dv=FAKE * 64 + nq + nkv, B=B, Hq=Hq, Hkv=Hkv, Sq=S, Sk=S, D=D,
+                softmax_scale=0.088, causal=1, window_left=-1, window_right=-1, softcap=0.0, dtype=0,
+                workspace=FAKE * 128, workspace_bytes=ws_need)
+
+    def call(**change):
+        a = dict(base)
+        a.update(change)
+        prm = g._BwdParams(**a)
+        return L.attn_bwd(ctypes.byref(prm))
+
+    assert L.attn_bwd(None) == 1
+    assert call(q=None) == 1
+    assert call(workspace=None) == 1
+    assert call(workspace_bytes=ws_need - 1) == 1
+    assert call(workspace=FAKE * 128 + 16) == 1          # workspace not 256-byte aligned
+    assert call(out=FAKE * 256) == 1                     # out without lse
+    assert call(Hkv=3) == 1                              # Hq % Hkv
+    assert call(causal=2) == 1
+    assert call(window_left=-2) == 1
+    assert call(D=96) == 2
+    assert call(dtype=1) == 2                            # fp32 backward not built
+    assert call(dq=FAKE) == 1                            # dq aliasing q
+    assert call(dv=FAKE * 64 + 8) == 1                   # dv overlapping dq (and misaligned)
+    assert call(dk=FAKE * 128) == 1                      # dk inside the workspace

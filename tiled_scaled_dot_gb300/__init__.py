@@ -24,7 +24,7 @@ import threading
 import torch
 
 __all__ = ["attn_fwd", "attn_fwd_varlen", "attn_decode", "decode_workspace_size", "attn_decode_paged",
-           "decode_paged_workspace_size", "device_status", "set_wait_timeout_ns",
+           "decode_paged_workspace_size", "attn_bwd", "bwd_workspace_size", "device_status", "set_wait_timeout_ns",
            "diag_umma", "diag_wait_timeout", "GbattnError", "lib", "LIB_PATH"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -51,6 +51,19 @@ class _FwdParams(ctypes.Structure):
                 ("Sk", ctypes.c_int), ("D", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("causal", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
                 ("softcap", ctypes.c_float), ("dtype", ctypes.c_int), ("stream", ctypes.c_void_p)]
+
+
+class _BwdParams(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("dout", ctypes.c_void_p),
+                ("alibi_slopes", ctypes.c_void_p), ("row_kv_bounds", ctypes.c_void_p),
+                ("dq", ctypes.c_void_p), ("dk", ctypes.c_void_p), ("dv", ctypes.c_void_p),
+                ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("Sq", ctypes.c_int),
+                ("Sk", ctypes.c_int), ("D", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+                ("causal", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+                ("softcap", ctypes.c_float), ("dtype", ctypes.c_int),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("stream", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -81,6 +94,10 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_paged_workspace_size.restype = Z
             L.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, P, Z, I, P]
             L.attn_decode_paged.restype = I
+            L.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            L.attn_bwd_workspace_size.restype = Z
+            L.attn_bwd.argtypes = [ctypes.POINTER(_BwdParams)]
+            L.attn_bwd.restype = I
             L.gbattn_status_string.argtypes = [I]
             L.gbattn_status_string.restype = ctypes.c_char_p
             L.gbattn_device_status.argtypes = [P, I]
@@ -310,6 +327,69 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slop
     if st:
         raise GbattnError(st, "attn_decode_paged")
     return out
+
+
+def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, recompute=True) -> int:
+    return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, int(bool(recompute))))
+
+
+def attn_bwd(q, k, v, dout, out=None, lse=None, alibi_slopes=None, *, softmax_scale=None, causal=False,
+             window_left=None, window_right=None, softcap=None, row_kv_bounds=None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Attention backward by recompute.  q, dout [B,Hq,Sq,D], k/v [B,Hkv,Sk,D]
+    (bf16 or fp16, CUDA); the forward's flags.
+
+    out and lse: the forward's output and fp32 lse [B,Hq,Sq] (attn_fwd with
+    lse=...), both or neither; when neither, the library recomputes them into
+    the workspace.  workspace: optional uint8 CUDA tensor of at least
+    bwd_workspace_size(...) bytes, allocated here (through torch) when None.
+    Returns (dq [B,Hq,Sq,D], dk [B,Hkv,Sk,D], dv [B,Hkv,Sk,D]) of q's dtype.
+    """
+    if q.dtype not in _DT16:
+        raise TypeError(f"attn_bwd takes bf16 or fp16, got {q.dtype}")
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _check(t, n, q.dtype, 4)
+    B, Hq, Sq, D = q.shape
+    Bk, Hkv, Sk, Dk = k.shape
+    if tuple(v.shape) != tuple(k.shape) or Bk != B or Dk != D or dout.shape != q.shape:
+        raise ValueError("k, v [B, Hkv, Sk, D]; dout of q's shape")
+    if (out is None) != (lse is None):
+        raise ValueError("give both out and lse, or neither")
+    if out is not None:
+        _check(out, "out", q.dtype, 4)
+        _check(lse, "lse", torch.float32, 3)
+        if out.shape != q.shape or tuple(lse.shape) != (B, Hq, Sq):
+            raise ValueError("out [B, Hq, Sq, D] and lse [B, Hq, Sq]")
+    if alibi_slopes is not None:
+        _check(alibi_slopes, "alibi_slopes", torch.float32, 1)
+        if alibi_slopes.numel() != Hq:
+            raise ValueError("alibi_slopes must be [Hq]")
+    if row_kv_bounds is not None:
+        _check(row_kv_bounds, "row_kv_bounds", torch.int32, 3)
+        if tuple(row_kv_bounds.shape) != (B, Sq, 2):
+            raise ValueError("row_kv_bounds must be [B, Sq, 2]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, n, like in ((dq, "dq", q), (dk, "dk", k), (dv, "dv", v)):
+        _check(t, n, q.dtype, 4)
+        if t.shape != like.shape:
+            raise ValueError(f"{n} must have the shape of its input")
+    need = bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, out is None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    else:
+        _check(workspace, "workspace", torch.uint8, 1)
+    scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
+    prm = _BwdParams(q.data_ptr(), k.data_ptr(), v.data_ptr(), _ptr(out), _ptr(lse), dout.data_ptr(),
+                     _ptr(alibi_slopes), _ptr(row_kv_bounds), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                     B, Hq, Hkv, Sq, Sk, D, scale, int(bool(causal)), _win(window_left), _win(window_right),
+                     float(softcap or 0.0), _DT[q.dtype], workspace.data_ptr(), workspace.numel(),
+                     _stream_handle(stream).value)
+    st = lib().attn_bwd(ctypes.byref(prm))
+    if st:
+        raise GbattnError(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def device_status(stream=None, clear: bool = True) -> int:

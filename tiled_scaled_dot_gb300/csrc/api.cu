@@ -308,6 +308,147 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* 
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
 
+// Backward workspace: base-2 lse and Delta per padded query row, row
+// intervals and tile summaries, then (recompute only) the forward's lse and
+// output.  Every region starts on a 256-byte boundary.
+struct BwdLayout {
+    size_t lse2, delta, rows, summ, lse, out, total;
+};
+static BwdLayout bwd_layout(int B, int Hq, int Sq, int D, bool recompute) {
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t sp = backward_sq_pad(Sq), nqt = ((size_t)Sq + 127) / 128;
+    BwdLayout L{};
+    size_t o = 0;
+    L.lse2 = o;
+    o += up((size_t)B * Hq * sp * 4);
+    L.delta = o;
+    o += up((size_t)B * Hq * sp * 4);
+    L.rows = o;
+    o += up((size_t)B * sp * 8);
+    L.summ = o;
+    o += up((size_t)B * nqt * 16);
+    if (recompute) {
+        L.lse = o;
+        o += up((size_t)B * Hq * Sq * 4);
+        L.out = o;
+        o += up((size_t)B * Hq * Sq * D * 2);
+    }
+    L.total = o;
+    return L;
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int recompute) {
+    if (check_common(B, Hq, Hkv, Sq, Sk, D, 1.f, 0.f, GBATTN_BF16)) return 0;
+    return bwd_layout(B, Hq, Sq, D, recompute != 0).total;
+}
+
+int attn_bwd(const gbattn_bwd_params* a) {
+    if (!a) return GBATTN_ERR_INVALID_ARG;
+    int rc = check_common(a->B, a->Hq, a->Hkv, a->Sq, a->Sk, a->D, a->softmax_scale, a->softcap, a->dtype);
+    if (rc) return rc;
+    if (a->dtype == GBATTN_F32) return GBATTN_ERR_UNSUPPORTED;
+    if (a->B > 65535) return GBATTN_ERR_UNSUPPORTED;  // batch is a grid dimension of the row-interval launch
+    if (!a->q || !a->k || !a->v || !a->dout || !a->dq || !a->dk || !a->dv || !a->workspace)
+        return GBATTN_ERR_INVALID_ARG;
+    if ((a->out == nullptr) != (a->lse == nullptr)) return GBATTN_ERR_INVALID_ARG;
+    if (a->causal != 0 && a->causal != 1) return GBATTN_ERR_INVALID_ARG;
+    if (a->window_left < -1 || a->window_right < -1) return GBATTN_ERR_INVALID_ARG;
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->dout) ||
+        (a->out && !aligned16(a->out)) || !aligned16(a->dq) || !aligned16(a->dk) || !aligned16(a->dv))
+        return GBATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return GBATTN_ERR_INVALID_ARG;
+    if (a->row_kv_bounds && (reinterpret_cast<uintptr_t>(a->row_kv_bounds) & 7u)) return GBATTN_ERR_INVALID_ARG;
+    if (a->lse && (reinterpret_cast<uintptr_t>(a->lse) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
+    const bool rec = a->out == nullptr;
+    const BwdLayout L = bwd_layout(a->B, a->Hq, a->Sq, a->D, rec);
+    if (a->workspace_bytes < L.total) return GBATTN_ERR_INVALID_ARG;
+    const size_t nq = (size_t)a->B * a->Hq * a->Sq * a->D * 2;
+    const size_t nkv = (size_t)a->B * a->Hkv * a->Sk * a->D * 2;
+    const void* ins[5] = {a->q, a->k, a->v, a->dout, a->out};
+    const size_t ins_n[5] = {nq, nkv, nkv, nq, nq};
+    void* grads[3] = {a->dq, a->dk, a->dv};
+    const size_t grads_n[3] = {nq, nkv, nkv};
+    for (int g = 0; g < 3; ++g) {
+        for (int i = 0; i < 5; ++i)
+            if (overlaps(grads[g], grads_n[g], ins[i], ins_n[i])) return GBATTN_ERR_INVALID_ARG;
+        for (int h = g + 1; h < 3; ++h)
+            if (overlaps(grads[g], grads_n[g], grads[h], grads_n[h])) return GBATTN_ERR_INVALID_ARG;
+        if (overlaps(grads[g], grads_n[g], a->workspace, L.total)) return GBATTN_ERR_INVALID_ARG;
+    }
+
+    BwdProblem b{};
+    if (!device_facts(&b.status, &b.num_sms)) return GBATTN_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+    const void* out = a->out;
+    const float* lse = a->lse;
+    if (rec) {
+        // recompute the forward's output and lse into the workspace
+        gbattn_fwd_params f{};
+        f.q = a->q;
+        f.k = a->k;
+        f.v = a->v;
+        f.alibi_slopes = a->alibi_slopes;
+        f.row_kv_bounds = a->row_kv_bounds;
+        f.out = ws + L.out;
+        f.lse_out = reinterpret_cast<float*>(ws + L.lse);
+        f.B = a->B;
+        f.Hq = a->Hq;
+        f.Hkv = a->Hkv;
+        f.Sq = a->Sq;
+        f.Sk = a->Sk;
+        f.D = a->D;
+        f.softmax_scale = a->softmax_scale;
+        f.causal = a->causal;
+        f.window_left = a->window_left;
+        f.window_right = a->window_right;
+        f.softcap = a->softcap;
+        f.dtype = a->dtype;
+        f.stream = a->stream;
+        rc = attn_fwd_ex(&f);
+        if (rc) return rc;
+        out = f.out;
+        lse = f.lse_out;
+    }
+    b.q = a->q;
+    b.k = a->k;
+    b.v = a->v;
+    b.out = out;
+    b.lse = lse;
+    b.dout = a->dout;
+    b.slopes = a->alibi_slopes;
+    b.row_bounds = a->row_kv_bounds;
+    b.dq = a->dq;
+    b.dk = a->dk;
+    b.dv = a->dv;
+    b.B = a->B;
+    b.Hq = a->Hq;
+    b.Hkv = a->Hkv;
+    b.Sq = a->Sq;
+    b.Sk = a->Sk;
+    b.D = a->D;
+    b.scale = a->softmax_scale;
+    b.causal = a->causal;
+    b.wl = a->window_left;
+    b.wr = a->window_right;
+    b.softcap = a->softcap;
+    b.f16 = a->dtype == GBATTN_F16;
+    b.ws_lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    b.ws_delta = reinterpret_cast<float*>(ws + L.delta);
+    b.ws_rows = reinterpret_cast<int32_t*>(ws + L.rows);
+    b.ws_summ = reinterpret_cast<int32_t*>(ws + L.summ);
+    b.timeout_ns = g_timeout_ns;
+    const bool h = b.f16 != 0;
+    CUtensorMap tq, tdo, tk, tv;
+    if (!cached_map(&tq, a->q, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h) ||
+        !cached_map(&tdo, a->dout, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h) ||
+        !cached_map(&tk, a->k, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h) ||
+        !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h))
+        return GBATTN_ERR_CUDA;
+    cudaError_t e = launch_backward_bf16(b, tq, tdo, tk, tv, static_cast<cudaStream_t>(a->stream));
+    return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
 static int decode_plan(int B, int Hq, int Hkv, int Sk, int D, int num_splits, int* splits, int* chunk) {
     if (check_common(B, Hq, Hkv, 1, Sk, D, 1.f, 0.f, GBATTN_BF16)) return -1;
     if (num_splits < 0) return -1;

@@ -1,0 +1,838 @@
+// backward_bf16.cu -- attention backward by recompute on tcgen05 tensor cores
+// (sm_103a), 16-bit inputs (bf16, or fp16 with the F16 flag), dense
+// [B, H, S, D] problems.
+//
+// Computes the gradients of attention.fkc.md, "attention_flash_backward":
+// with P the forward's softmax recomputed from Q, K and the forward's lse,
+//   dV_j = sum_i P_ij dO_i,   dP_ij = dO_i . V_j,
+//   dS_ij = P_ij (dP_ij - Delta_i) [* (1 - tanh^2(s_pre / c)) with softcap],
+//   dQ_i = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i,
+// where Delta_i = sum_j P_ij dP_ij = dO_i . O_i (O the forward output), and
+// dK / dV of a kv head sum over the query heads of its GQA group.
+//
+// Three launches, all deterministic (no atomics, fixed summation order):
+//   bwd_rows_kernel    per query row its admissible key interval [a, e]
+//                      (causal, window, row bounds, Sk) and per 128-row query
+//                      tile a summary: the span of its live rows' intervals
+//                      and the tightest interval common to all its rows;
+//   bwd_delta_kernel   per (b, h, row) Delta = dO . O and the base-2 lse
+//                      (+inf for a row with no admissible key, so P = 0);
+//   bwd_kernel<DQ=0>   one work item per (b, kv head, 128-key tile): S^T =
+//                      K Q^T and dP^T = V dO^T for every admissible 128-row
+//                      query tile of every head of the group, dV += P^T dO
+//                      and dK += dS^T Q accumulated in TMEM;
+//   bwd_kernel<DQ=1>   one work item per (b, head, 128-row query tile): S =
+//                      Q K^T, dP = dO V^T for every admissible key tile,
+//                      dQ += dS K accumulated in TMEM.
+// The two main launches are one template: a pair of "fixed" tiles per item
+// (K, V or Q, dO) stays in shared memory while pairs of "streamed" tiles
+// (Q, dO or K, V) move through an NSTG-stage ring; both products S and dP take
+// the fixed tile as A (M = 128 lanes) and the streamed tile as B (N = 128).
+//
+// Structure (10 warps, one persistent CTA per SM):
+//   WG0, WG1 (warps 0-7)   element-wise: thread (g, r) owns TMEM lane r and
+//                          columns 64 g .. 64 g + 63 of S and dP; writes P
+//                          (DQ = 0) and dS as 16-bit into TMEM; at the end of
+//                          an item reads the accumulators out (scale, round,
+//                          store)
+//   warp 8                 TMA producer
+//   warp 9                 MMA issuer (one elected lane issues)
+// TMEM (512 columns): S / P at 0, dP / dS at 128, accumulators at 256
+// (dV or dQ) and 256 + D (dK).  Packed 16-bit P and dS of group g sit at
+// columns 64 g .. 64 g + 31 of their tile, so neither group overwrites
+// fp32 values the other has not read yet.
+//
+// MMA order, DQ = 0 (item with steps 0 .. J-1):
+//   S_0, dP_0, then per step j: [P_j] dV += P_j dO_j, S_{j+1},
+//   [dS_j] dK += dS_j Q_j, dP_{j+1}
+// DQ = 1:
+//   S_0, dP_0, then per step j: [S_j read] S_{j+1}, [dS_j] dQ += dS_j K_j, dP_{j+1}
+// ([x] = wait for the element-wise warps).  tcgen05 operations issued by one
+// thread execute in order, so an MMA that overwrites a TMEM tile is issued
+// after the MMA that reads the tile's previous contents.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int TR = 128;  // rows of every tile (query rows or keys)
+constexpr int NUM_WARPS = 10;
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int EW_THREADS = 256;
+constexpr int WARP_PRODUCER = 8;
+constexpr int WARP_MMA = 9;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int EXTRA_BYTES = 2048;  // per stage (DQ = 0): lse2[128], delta[128], rows int2[128]
+
+template <int D>
+struct BCfg {
+    static constexpr int HALVES = D / 64;
+    static constexpr int TILE_BYTES = TR * D * 2;
+    static constexpr int SLAB = TR * 128;  // one 64-column slab of a tile
+    static constexpr int NSTG = (D == 128) ? 2 : 4;
+    static constexpr int SMEM_BYTES = 2 * TILE_BYTES + NSTG * 2 * TILE_BYTES + NSTG * EXTRA_BYTES + 1024;
+    static constexpr uint32_t ACC1 = 256;      // dV (DQ = 0) or dQ (DQ = 1)
+    static constexpr uint32_t ACC2 = 256 + D;  // dK (DQ = 0)
+};
+
+struct BParams {
+    uint16_t* dq;  // [B, Hq, Sq, D]
+    uint16_t* dk;  // [B, Hkv, Sk, D]
+    uint16_t* dv;  // [B, Hkv, Sk, D]
+    const float* lse2;   // [B * Hq][Sq_pad] base-2 lse (+inf: no admissible key, or padding)
+    const float* delta;  // [B * Hq][Sq_pad]
+    const int2* rows;    // [B][Sq_pad] admissible key interval of each query row
+    const int4* summ;    // [B][n_qt] per query tile: (lo_live, hi_live, a_max, e_min)
+    const float* slopes;
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    int B, Hq, Hkv, Sq, Sk, G, Sq_pad, n_qt, n_kt;
+    int causal;
+    float scale;       // softmax_scale (dQ, dK)
+    float scale_log2;  // softmax_scale * log2(e)
+    float cap_in;      // softmax_scale / softcap
+    float cap_out;     // softcap * log2(e)
+    int n_items;
+};
+
+__device__ __forceinline__ int item_of(int k, int cta, int grid) {
+    return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <bool F16>
+__device__ __forceinline__ float widen16(uint16_t x) {
+    return F16 ? __half2float(__ushort_as_half(x)) : __uint_as_float(static_cast<uint32_t>(x) << 16);
+}
+
+// ---------------------------------------------------------------------------- row intervals
+// Grid (n_qt, B), 128 threads: thread r handles query row m * 128 + r.
+__global__ void __launch_bounds__(TR) bwd_rows_kernel(const int2* __restrict__ rowb, int2* __restrict__ rows,
+                                                      int4* __restrict__ summ, int Sq, int Sk, int Sq_pad,
+                                                      int n_qt, int causal, int wl, int wr) {
+    const int m = blockIdx.x, b = blockIdx.y, r = threadIdx.x;
+    const int i = m * TR + r;
+    long long a = 0, e = Sk - 1;
+    if (causal) e = e < i ? e : i;
+    if (wl >= 0) a = a > (long long)i - wl ? a : (long long)i - wl;
+    if (wr >= 0) e = e < (long long)i + wr ? e : (long long)i + wr;
+    if (i < Sq && rowb) {
+        const int2 rb = rowb[(size_t)b * Sq + i];
+        a = a > rb.x ? a : rb.x;
+        e = e < rb.y ? e : rb.y;
+    }
+    const bool live = i < Sq && a <= e;
+    if (!live) {
+        a = 1;
+        e = 0;
+    }
+    rows[(size_t)b * Sq_pad + i] = make_int2((int)a, (int)e);
+    int lo = live ? (int)a : 0x7fffffff, hi = live ? (int)e : -1;
+    int amax = live ? (int)a : 0x7fffffff, emin = live ? (int)e : -1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
+    }
+    __shared__ int4 red[TR / 32];
+    if ((r & 31) == 0) red[r >> 5] = make_int4(lo, hi, amax, emin);
+    __syncthreads();
+    if (r == 0) {
+        int4 s = red[0];
+        for (int w = 1; w < TR / 32; ++w) {
+            s.x = min(s.x, red[w].x);
+            s.y = max(s.y, red[w].y);
+            s.z = max(s.z, red[w].z);
+            s.w = min(s.w, red[w].w);
+        }
+        summ[(size_t)b * n_qt + m] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------- Delta and base-2 lse
+// One warp per padded row (b h, i): Delta = dO . O in fp32, lse2 = lse * log2(e).
+template <int D, bool F16>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ dout,
+                                                        const uint16_t* __restrict__ out,
+                                                        const float* __restrict__ lse, float* __restrict__ lse2,
+                                                        float* __restrict__ delta, long long n_rows, int Sq,
+                                                        int Sq_pad) {
+    constexpr int PER = D / 32;  // elements per lane
+    const int lane = threadIdx.x & 31;
+    const long long w0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long row = w0; row < n_rows; row += nw) {
+        const long long bh = row / Sq_pad;
+        const int i = (int)(row - bh * Sq_pad);
+        float d = 0.f, l2 = INFINITY;
+        if (i < Sq) {
+            const size_t off = ((size_t)bh * Sq + i) * D + lane * PER;
+            uint16_t a[PER], c[PER];
+            if (PER == 4) {
+                *reinterpret_cast<uint2*>(a) = *reinterpret_cast<const uint2*>(dout + off);
+                *reinterpret_cast<uint2*>(c) = *reinterpret_cast<const uint2*>(out + off);
+            } else {
+                *reinterpret_cast<uint32_t*>(a) = *reinterpret_cast<const uint32_t*>(dout + off);
+                *reinterpret_cast<uint32_t*>(c) = *reinterpret_cast<const uint32_t*>(out + off);
+            }
+#pragma unroll
+            for (int t = 0; t < PER; ++t) d = fmaf(widen16<F16>(a[t]), widen16<F16>(c[t]), d);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            const float l = lse[(size_t)bh * Sq + i];
+            l2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
+        }
+        if (lane == 0) {
+            lse2[row] = l2;
+            delta[row] = d;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------- work items
+// DQ = 0: item -> (b, kv head, key tile n), lowest n first (under a top-left
+// causal mask the first key tiles meet the most query tiles).
+// DQ = 1: item -> (b, query head, query tile m), last m first under causal.
+struct BItem {
+    int b, hd, t;
+};
+
+template <bool DQ>
+__device__ __forceinline__ BItem bwd_item(const BParams& p, int item) {
+    const int heads = DQ ? p.Hq : p.Hkv;
+    const int per = p.B * heads;
+    const int tr = item / per, rest = item - tr * per;
+    BItem it;
+    it.b = rest / heads;
+    it.hd = rest - it.b * heads;
+    it.t = (DQ && p.causal) ? (p.n_qt - 1 - tr) : tr;
+    return it;
+}
+
+// DQ = 0: does query tile m hold a row whose interval meets keys [k0, k1]?
+__device__ __forceinline__ bool tile_meets(const int4& s, int k0, int k1) { return s.x <= k1 && s.y >= k0; }
+
+// DQ = 0: range [m_lo, m_hi] of query tiles that meet the key tile (m_lo > m_hi: none).
+__device__ __forceinline__ void q_tile_range(const BParams& p, int b, int k0, int k1, int& m_lo, int& m_hi) {
+    m_lo = 0x7fffffff;
+    m_hi = -1;
+    const int4* s = p.summ + (size_t)b * p.n_qt;
+    for (int m = 0; m < p.n_qt; ++m) {
+        if (tile_meets(__ldg(s + m), k0, k1)) {
+            m_lo = min(m_lo, m);
+            m_hi = m;
+        }
+    }
+}
+
+// DQ = 1: range [n_lo, n_hi] of key tiles of query tile m (n_lo > n_hi: none).
+__device__ __forceinline__ void k_tile_range(const BParams& p, int b, int m, int& n_lo, int& n_hi) {
+    const int4 s = __ldg(p.summ + (size_t)b * p.n_qt + m);
+    if (s.x <= s.y) {
+        n_lo = s.x / TR;
+        n_hi = s.y / TR;
+    } else {
+        n_lo = 0;
+        n_hi = -1;
+    }
+}
+
+struct BSmem {
+    uint64_t fix_full, fix_empty;
+    uint64_t stg_full[4], stg_empty[4];
+    uint64_t s_full, dp_full, p_full, s_free, ds_full, acc_full, acc_empty;
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// The steps of an item, enumerated the same way by every role.
+//   DQ = 0: for each head of the group, each query tile in [m_lo, m_hi] that
+//           meets the key tile; f(h, m).
+//   DQ = 1: each key tile n in [n_lo, n_hi]; f(n).
+// f returns false to stop.
+template <bool DQ, typename F>
+__device__ __forceinline__ bool for_steps(const BParams& p, const BItem& it, F&& f) {
+    if (DQ) {
+        int n_lo, n_hi;
+        k_tile_range(p, it.b, it.t, n_lo, n_hi);
+        for (int n = n_lo; n <= n_hi; ++n)
+            if (!f(it.hd, n)) return false;
+    } else {
+        const int k0 = it.t * TR, k1 = min(k0 + TR - 1, p.Sk - 1);
+        int m_lo, m_hi;
+        q_tile_range(p, it.b, k0, k1, m_lo, m_hi);
+        const int4* s = p.summ + (size_t)it.b * p.n_qt;
+        for (int hh = 0; hh < p.G; ++hh)
+            for (int m = m_lo; m <= m_hi; ++m)
+                if (tile_meets(__ldg(s + m), k0, k1) && !f(it.hd * p.G + hh, m)) return false;
+    }
+    return true;
+}
+
+template <bool DQ>
+__device__ __forceinline__ int count_steps(const BParams& p, const BItem& it) {
+    int n = 0;
+    for_steps<DQ>(p, it, [&](int, int) {
+        ++n;
+        return true;
+    });
+    return n;
+}
+
+// ---------------------------------------------------------------------------- element-wise role
+// Store 32 fp32 accumulator values (times f) of one output row as 16-bit.
+template <bool F16>
+__device__ __forceinline__ void store_row32(uint16_t* dst, const float (&v)[32], float f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint4 w;
+        w.x = pack16x2<F16>(v[8 * i + 0] * f, v[8 * i + 1] * f);
+        w.y = pack16x2<F16>(v[8 * i + 2] * f, v[8 * i + 3] * f);
+        w.z = pack16x2<F16>(v[8 * i + 4] * f, v[8 * i + 5] * f);
+        w.w = pack16x2<F16>(v[8 * i + 6] * f, v[8 * i + 7] * f);
+        reinterpret_cast<uint4*>(dst)[i] = w;
+    }
+}
+
+__device__ __forceinline__ void zero_row(uint16_t* dst, int n) {
+    for (int i = 0; i < n / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+}
+
+template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
+__device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tmem, const WaitCtl& wc, int warp,
+                                        const uint8_t* sX) {
+    using C = BCfg<D>;
+    const int g = warp >> 2;          // column group: columns 64 g .. 64 g + 63
+    const int r = threadIdx.x & (TR - 1);  // TMEM lane
+    const int c0 = 64 * g;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + c0;         // S; packed P at its first 32 columns
+    const uint32_t tDP = tmem + lane_off + 128 + c0;  // dP; packed dS at its first 32 columns
+    const int grid = gridDim.x, cta = blockIdx.x;
+    uint32_t step = 0, acc_cnt = 0, stg = 0;
+    for (int k = 0;; ++k) {
+        const int item = item_of(k, cta, grid);
+        if (item >= p.n_items) break;
+        const BItem it = bwd_item<DQ>(p, item);
+        const int J = count_steps<DQ>(p, it);
+        if (J == 0) {
+            // no admissible (row, key) pair touches the item: zero gradient rows
+            if (DQ) {
+                const int i = it.t * TR + r;
+                if (i < p.Sq) zero_row(p.dq + ((size_t)(it.b * p.Hq + it.hd) * p.Sq + i) * D + g * (D / 2), D / 2);
+            } else {
+                const int key = it.t * TR + r;
+                if (key < p.Sk) zero_row((g ? p.dk : p.dv) + ((size_t)(it.b * p.Hkv + it.hd) * p.Sk + key) * D, D);
+            }
+            continue;
+        }
+        // DQ = 1: this thread's query row, fixed over the item
+        int ra = 1, rb = 0;
+        float lse2_i = INFINITY, delta_i = 0.f;
+        if (DQ) {
+            const int i = it.t * TR + r;  // < Sq_pad
+            const int2 iv = __ldg(p.rows + (size_t)it.b * p.Sq_pad + i);
+            ra = iv.x;
+            rb = iv.y;
+            lse2_i = __ldg(p.lse2 + (size_t)(it.b * p.Hq + it.hd) * p.Sq_pad + i);
+            delta_i = __ldg(p.delta + (size_t)(it.b * p.Hq + it.hd) * p.Sq_pad + i);
+        }
+        const bool ok = for_steps<DQ>(p, it, [&](int h, int u) -> bool {
+            const int st = (int)(stg % C::NSTG);
+            const uint32_t sp = (stg / C::NSTG) & 1u;
+            ++stg;
+            bool w = true;
+            // DQ = 0: admissible columns of this thread's key as a bit mask, from
+            // the stage's row intervals (all ones when every row admits the tile)
+            uint64_t adm = ~0ull;
+            if (!DQ) {
+                w = mbar_wait(&sm.stg_full[st], sp, wc, ST_BWD_EW);
+                const int k0 = it.t * TR, kj = k0 + r;
+                const int4 su = __ldg(p.summ + (size_t)it.b * p.n_qt + u);
+                if (w && !(su.z <= k0 && su.w >= k0 + TR - 1)) {
+                    const int4* xr = reinterpret_cast<const int4*>(sX + st * EXTRA_BYTES + 1024) + c0 / 2;
+                    adm = 0ull;
+#pragma unroll 8
+                    for (int c = 0; c < 64; c += 2) {
+                        const int4 iv = xr[c >> 1];  // intervals of columns c, c + 1
+                        const uint64_t two = (uint64_t)(kj >= iv.x && kj <= iv.y) | ((uint64_t)(kj >= iv.z && kj <= iv.w) << 1);
+                        adm |= two << c;
+                    }
+                }
+            }
+            w = w && mbar_wait(&sm.s_full, step & 1u, wc, ST_BWD_EW);
+            if (!__all_sync(0xffffffffu, w)) return false;
+            tc_fence_after();
+            float sv[64];
+            tmem_ld64(tS, sv);
+            if (DQ) {
+                // S is in registers: the next S may overwrite the tile
+                tc_fence_before();
+                mbar_arrive(&sm.s_free);
+            }
+            const float slope_l2 = ALIBI ? __ldg(p.slopes + h) * LOG2E : 0.f;
+            uint32_t pw[32];
+            if (!DQ) {
+                // thread = key kj, columns = query rows i = m * 128 + c0 + c
+                const float* xl = reinterpret_cast<const float*>(sX + st * EXTRA_BYTES) + c0;  // lse2
+                const int kj = it.t * TR + r;
+                const float abase = ALIBI ? slope_l2 * (float)(kj - u * TR - c0) : 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    float z[2], f[2] = {1.f, 1.f};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (SOFTCAP) {
+                            const float t = tanh_approx(sv[c + e] * p.cap_in);
+                            z[e] = p.cap_out * t;
+                            f[e] = fmaf(-t, t, 1.f);
+                        } else {
+                            z[e] = sv[c + e] * p.scale_log2;
+                        }
+                        if (ALIBI) z[e] += fmaf(-slope_l2, (float)(c + e), abase);
+                        const float pe = ex2_approx(z[e] - xl[c + e]);
+                        z[e] = ((adm >> (c + e)) & 1ull) ? pe : 0.f;
+                    }
+                    pw[c >> 1] = pack16x2<F16>(z[0], z[1]);
+                    sv[c] = z[0] * f[0];
+                    sv[c + 1] = z[1] * f[1];
+                }
+                tmem_st32(tS, pw);
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.p_full);
+            } else {
+                // thread = query row i, columns = keys k0 + c0 + c
+                const int i = it.t * TR + r;
+                const int kb = u * TR + c0;
+                const int lo = ra - kb, hi = rb - kb;
+                const bool need = kb < ra || kb + 63 > rb;
+                const float abase = ALIBI ? slope_l2 * (float)(kb - i) : 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    float z, f = 1.f;
+                    if (SOFTCAP) {
+                        const float t = tanh_approx(sv[c] * p.cap_in);
+                        z = p.cap_out * t;
+                        f = fmaf(-t, t, 1.f);
+                    } else {
+                        z = sv[c] * p.scale_log2;
+                    }
+                    if (ALIBI) z += fmaf(slope_l2, (float)c, abase);
+                    float pe = ex2_approx(z - lse2_i);
+                    if (need) pe = (c < lo || c > hi) ? 0.f : pe;
+                    sv[c] = pe * f;
+                }
+            }
+            w = mbar_wait(&sm.dp_full, step & 1u, wc, ST_BWD_EW);
+            if (!__all_sync(0xffffffffu, w)) return false;
+            tc_fence_after();
+            // dS in two 32-column halves (both read before the packed store
+            // overwrites the first half's columns)
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                float dp[32];
+                tmem_ld32(tDP + 32 * hf, dp);
+                if (!DQ) {
+                    const float* xd = reinterpret_cast<const float*>(sX + st * EXTRA_BYTES + 512) + c0 + 32 * hf;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2)
+                        pw[16 * hf + (c >> 1)] = pack16x2<F16>(sv[32 * hf + c] * (dp[c] - xd[c]),
+                                                               sv[32 * hf + c + 1] * (dp[c + 1] - xd[c + 1]));
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2)
+                        pw[16 * hf + (c >> 1)] = pack16x2<F16>(sv[32 * hf + c] * (dp[c] - delta_i),
+                                                               sv[32 * hf + c + 1] * (dp[c + 1] - delta_i));
+                }
+            }
+            tmem_st32(tDP, pw);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&sm.ds_full);
+            ++step;
+            return true;
+        });
+        if (!ok) return;
+        // the item's accumulators: read, scale, round, store
+        const bool w = mbar_wait(&sm.acc_full, acc_cnt & 1u, wc, ST_BWD_EW);
+        ++acc_cnt;
+        if (!__all_sync(0xffffffffu, w)) return;
+        tc_fence_after();
+        if (DQ) {
+            const int i = it.t * TR + r;
+            uint16_t* dst = p.dq + ((size_t)(it.b * p.Hq + it.hd) * p.Sq + i) * D + g * (D / 2);
+#pragma unroll
+            for (int c = 0; c < D / 2; c += 32) {
+                float v[32];
+                tmem_ld32(tmem + lane_off + C::ACC1 + g * (D / 2) + c, v);
+                if (i < p.Sq) store_row32<F16>(dst + c, v, p.scale);
+            }
+        } else {
+            const int key = it.t * TR + r;
+            uint16_t* dst = (g ? p.dk : p.dv) + ((size_t)(it.b * p.Hkv + it.hd) * p.Sk + key) * D;
+            const uint32_t acc = g ? C::ACC2 : C::ACC1;
+            const float f = g ? p.scale : 1.f;
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+                float v[32];
+                tmem_ld32(tmem + lane_off + acc + c, v);
+                if (key < p.Sk) store_row32<F16>(dst + c, v, f);
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&sm.acc_empty);
+    }
+}
+
+// ---------------------------------------------------------------------------- kernel
+template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BParams p) {
+    using C = BCfg<D>;
+    extern __shared__ __align__(1024) uint8_t dyn_smem[];
+    __shared__ BSmem sm;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
+    uint8_t* sF1 = base;                        // K (DQ = 0) or Q (DQ = 1)
+    uint8_t* sF2 = base + C::TILE_BYTES;        // V or dO
+    uint8_t* sT = base + 2 * C::TILE_BYTES;     // stage s: T1 (Q or K) at 2 s, T2 (dO or V) at 2 s + 1 tiles
+    uint8_t* sX = sT + C::NSTG * 2 * C::TILE_BYTES;  // stage extras (DQ = 0)
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.fix_full, 1);
+        mbar_init(&sm.fix_empty, 1);
+        for (int i = 0; i < C::NSTG; ++i) {
+            mbar_init(&sm.stg_full[i], 1);
+            mbar_init(&sm.stg_empty[i], 1);
+        }
+        mbar_init(&sm.s_full, 1);
+        mbar_init(&sm.dp_full, 1);
+        mbar_init(&sm.p_full, EW_THREADS);
+        mbar_init(&sm.s_free, EW_THREADS);
+        mbar_init(&sm.ds_full, EW_THREADS);
+        mbar_init(&sm.acc_full, 1);
+        mbar_init(&sm.acc_empty, EW_THREADS);
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == WARP_PRODUCER) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    WaitCtl wc{&sm.abort_flag, p.status, p.timeout_ns};
+    const int grid = gridDim.x, cta = blockIdx.x;
+
+    if (warp < 8) {
+        ew_role<D, DQ, SOFTCAP, ALIBI, F16>(p, sm, tmem, wc, warp, sX);
+    } else if (warp == WARP_PRODUCER) {
+        if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmDO);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            uint32_t fix_cnt = 0, stg = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k) {
+                const int item = item_of(k, cta, grid);
+                if (item >= p.n_items) break;
+                const BItem it = bwd_item<DQ>(p, item);
+                if (count_steps<DQ>(p, it) == 0) continue;
+                ok = mbar_wait(&sm.fix_empty, (fix_cnt & 1u) ^ 1u, wc, ST_BWD_PRODUCER);
+                if (!ok) break;
+                mbar_arrive_expect_tx(&sm.fix_full, 2 * C::TILE_BYTES);
+                const int hkv = DQ ? it.hd / p.G : it.hd;
+#pragma unroll
+                for (int hf = 0; hf < C::HALVES; ++hf) {
+                    if (DQ) {
+                        tma_load_3d(sF1 + hf * C::SLAB, &tmQ, &sm.fix_full, hf * 64, it.t * TR, it.b * p.Hq + it.hd);
+                        tma_load_3d(sF2 + hf * C::SLAB, &tmDO, &sm.fix_full, hf * 64, it.t * TR, it.b * p.Hq + it.hd);
+                    } else {
+                        tma_load_3d(sF1 + hf * C::SLAB, &tmK, &sm.fix_full, hf * 64, it.t * TR, it.b * p.Hkv + hkv);
+                        tma_load_3d(sF2 + hf * C::SLAB, &tmV, &sm.fix_full, hf * 64, it.t * TR, it.b * p.Hkv + hkv);
+                    }
+                }
+                ++fix_cnt;
+                ok = for_steps<DQ>(p, it, [&](int h, int u) -> bool {
+                    const int st = (int)(stg % C::NSTG);
+                    if (!mbar_wait(&sm.stg_empty[st], ((stg / C::NSTG) & 1u) ^ 1u, wc, ST_BWD_PRODUCER)) return false;
+                    uint64_t* fb = &sm.stg_full[st];
+                    mbar_arrive_expect_tx(fb, 2 * C::TILE_BYTES + (DQ ? 0 : EXTRA_BYTES));
+                    uint8_t* t1 = sT + st * 2 * C::TILE_BYTES;
+                    uint8_t* t2 = t1 + C::TILE_BYTES;
+#pragma unroll
+                    for (int hf = 0; hf < C::HALVES; ++hf) {
+                        if (DQ) {
+                            tma_load_3d(t1 + hf * C::SLAB, &tmK, fb, hf * 64, u * TR, it.b * p.Hkv + hkv);
+                            tma_load_3d(t2 + hf * C::SLAB, &tmV, fb, hf * 64, u * TR, it.b * p.Hkv + hkv);
+                        } else {
+                            tma_load_3d(t1 + hf * C::SLAB, &tmQ, fb, hf * 64, u * TR, it.b * p.Hq + h);
+                            tma_load_3d(t2 + hf * C::SLAB, &tmDO, fb, hf * 64, u * TR, it.b * p.Hq + h);
+                        }
+                    }
+                    if (!DQ) {
+                        const size_t row = (size_t)(it.b * p.Hq + h) * p.Sq_pad + (size_t)u * TR;
+                        uint8_t* x = sX + st * EXTRA_BYTES;
+                        bulk_load(x, p.lse2 + row, 512, fb);
+                        bulk_load(x + 512, p.delta + row, 512, fb);
+                        bulk_load(x + 1024, p.rows + (size_t)it.b * p.Sq_pad + (size_t)u * TR, 1024, fb);
+                    }
+                    ++stg;
+                    return true;
+                });
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA leaves
+                const uint32_t n = stg < (uint32_t)C::NSTG ? stg : (uint32_t)C::NSTG;
+                for (uint32_t i = stg - n; i < stg; ++i)
+                    mbar_drain(&sm.stg_full[i % C::NSTG], (i / C::NSTG) & 1u, 100000000ull);
+                if (fix_cnt) mbar_drain(&sm.fix_full, (fix_cnt - 1) & 1u, 100000000ull);
+            }
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // The whole warp runs the loop; one elected lane issues each MMA and
+        // commit.  Waits are warp votes, so the warp stays converged.
+        auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, ST_BWD_MMA));
+        };
+        constexpr uint32_t IDESC_S = F16 ? idesc_f16_f32(TR, TR, 0) : idesc_bf16_f32(TR, TR, 0);
+        constexpr uint32_t IDESC_A = F16 ? idesc_f16_f32(TR, D, 1) : idesc_bf16_f32(TR, D, 1);
+        const uint32_t aF1 = smem_u32(sF1), aF2 = smem_u32(sF2), aT = smem_u32(sT);
+        auto t1_of = [&](uint32_t s) { return aT + (s % C::NSTG) * 2 * C::TILE_BYTES; };
+        auto t2_of = [&](uint32_t s) { return aT + (s % C::NSTG) * 2 * C::TILE_BYTES + C::TILE_BYTES; };
+        // D[col] = A B^T over K = D: both operands K-major 128 x D tiles
+        auto mma_ss = [&](uint32_t col, uint32_t a, uint32_t b) {
+            const uint32_t alo = sdesc_lo(a, 16), blo = sdesc_lo(b, 16);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = ((kk >> 2) * C::SLAB + (kk & 3) * 32) >> 4;
+                umma_ss_lo_elect(tmem + col, alo + off, blo + off, IDESC_S, kk > 0 ? 1u : 0u);
+            }
+        };
+        // D[col] (+)= A[TMEM, packed 16-bit at acol] B over K = 128 rows of the
+        // MN-major 128 x D tile b
+        auto mma_ts = [&](uint32_t col, uint32_t acol, uint32_t b, uint32_t acc) {
+            const uint32_t blo = sdesc_lo(b, C::SLAB);
+#pragma unroll
+            for (int kk = 0; kk < TR / 16; ++kk) {
+                const uint32_t a = tmem + acol + ((kk < 4) ? 8u * kk : 64u + 8u * (kk - 4));
+                umma_ts_lo_elect(tmem + col, a, blo + ((kk * 16 * 128) >> 4), IDESC_A, kk > 0 ? 1u : acc);
+            }
+        };
+        uint32_t fix_cnt = 0, stg = 0, step = 0, acc_cnt = 0;
+        bool ok = true;
+        for (int k = 0; ok; ++k) {
+            const int item = item_of(k, cta, grid);
+            if (item >= p.n_items) break;
+            const BItem it = bwd_item<DQ>(p, item);
+            const int J = count_steps<DQ>(p, it);
+            if (J == 0) continue;
+            ok = wwait(&sm.fix_full, fix_cnt & 1u);
+            ++fix_cnt;
+            ok = ok && wwait(&sm.stg_full[stg % C::NSTG], (stg / C::NSTG) & 1u);
+            if (!ok) break;
+            tc_fence_after();
+            mma_ss(0, aF1, t1_of(stg));
+            umma_commit_elect(&sm.s_full);
+            mma_ss(128, aF2, t2_of(stg));
+            umma_commit_elect(&sm.dp_full);
+            for (int j = 0; j < J && ok; ++j, ++step) {
+                const uint32_t sj = stg + j, sn = sj + 1;
+                const bool more = j + 1 < J;
+                if (!DQ) {
+                    ok = wwait(&sm.p_full, step & 1u);
+                    if (ok && j == 0) ok = wwait(&sm.acc_empty, (acc_cnt & 1u) ^ 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_ts(C::ACC1, 0, t2_of(sj), j > 0 ? 1u : 0u);  // dV += P^T dO
+                    if (more) {
+                        if (!(ok = wwait(&sm.stg_full[sn % C::NSTG], (sn / C::NSTG) & 1u))) break;
+                        tc_fence_after();
+                        mma_ss(0, aF1, t1_of(sn));
+                        umma_commit_elect(&sm.s_full);
+                    }
+                    if (!(ok = wwait(&sm.ds_full, step & 1u))) break;
+                    tc_fence_after();
+                    mma_ts(C::ACC2, 128, t1_of(sj), j > 0 ? 1u : 0u);  // dK += dS^T Q
+                    umma_commit_elect(&sm.stg_empty[sj % C::NSTG]);
+                    if (more) {
+                        mma_ss(128, aF2, t2_of(sn));
+                        umma_commit_elect(&sm.dp_full);
+                    }
+                } else {
+                    if (more) {
+                        ok = wwait(&sm.s_free, step & 1u);
+                        ok = ok && wwait(&sm.stg_full[sn % C::NSTG], (sn / C::NSTG) & 1u);
+                        if (!ok) break;
+                        tc_fence_after();
+                        mma_ss(0, aF1, t1_of(sn));
+                        umma_commit_elect(&sm.s_full);
+                    }
+                    ok = wwait(&sm.ds_full, step & 1u);
+                    if (ok && j == 0) ok = wwait(&sm.acc_empty, (acc_cnt & 1u) ^ 1u);
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_ts(C::ACC1, 128, t1_of(sj), j > 0 ? 1u : 0u);  // dQ += dS K
+                    umma_commit_elect(&sm.stg_empty[sj % C::NSTG]);
+                    if (more) {
+                        mma_ss(128, aF2, t2_of(sn));
+                        umma_commit_elect(&sm.dp_full);
+                    }
+                }
+            }
+            if (!ok) break;
+            stg += J;
+            umma_commit_elect(&sm.acc_full);
+            umma_commit_elect(&sm.fix_empty);
+            ++acc_cnt;
+        }
+        if (lane == 0) {
+            // every MMA issued must finish before TMEM is released
+            umma_commit(&sm.drain);
+            mbar_drain(&sm.drain, 0, 100000000ull);
+        }
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_PRODUCER) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
+cudaError_t launch_main(const BParams& prm, int grid, const CUtensorMap& tq, const CUtensorMap& tdo,
+                        const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    auto kern = bwd_kernel<D, DQ, SOFTCAP, ALIBI, F16>;
+    const int smem = BCfg<D>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tdo, tk, tv, prm);
+    return cudaGetLastError();
+}
+
+template <int D, bool F16>
+cudaError_t launch_flags(const BParams& prm, int grid_a, int grid_b, bool cap, bool ali, const CUtensorMap& tq,
+                         const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    BParams pa = prm, pb = prm;
+    pa.n_items = prm.n_kt * prm.B * prm.Hkv;
+    pb.n_items = prm.n_qt * prm.B * prm.Hq;
+    cudaError_t e;
+#define GBATTN_BWD_PAIR(CAP, ALI)                                                              \
+    e = launch_main<D, false, CAP, ALI, F16>(pa, grid_a, tq, tdo, tk, tv, stream);              \
+    if (e != cudaSuccess) return e;                                                             \
+    return launch_main<D, true, CAP, ALI, F16>(pb, grid_b, tq, tdo, tk, tv, stream);
+    if (cap) {
+        if (ali) {
+            GBATTN_BWD_PAIR(true, true)
+        } else {
+            GBATTN_BWD_PAIR(true, false)
+        }
+    } else {
+        if (ali) {
+            GBATTN_BWD_PAIR(false, true)
+        } else {
+            GBATTN_BWD_PAIR(false, false)
+        }
+    }
+#undef GBATTN_BWD_PAIR
+}
+
+}  // namespace
+
+size_t backward_sq_pad(int Sq) { return ((size_t)Sq + TR - 1) / TR * TR; }
+
+cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, const CUtensorMap& tdo,
+                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+    BParams p{};
+    p.dq = static_cast<uint16_t*>(b.dq);
+    p.dk = static_cast<uint16_t*>(b.dk);
+    p.dv = static_cast<uint16_t*>(b.dv);
+    p.lse2 = b.ws_lse2;
+    p.delta = b.ws_delta;
+    p.rows = reinterpret_cast<const int2*>(b.ws_rows);
+    p.summ = reinterpret_cast<const int4*>(b.ws_summ);
+    p.slopes = b.slopes;
+    p.status = b.status;
+    p.timeout_ns = b.timeout_ns;
+    p.B = b.B;
+    p.Hq = b.Hq;
+    p.Hkv = b.Hkv;
+    p.Sq = b.Sq;
+    p.Sk = b.Sk;
+    p.G = b.Hq / b.Hkv;
+    p.Sq_pad = (int)backward_sq_pad(b.Sq);
+    p.n_qt = (b.Sq + TR - 1) / TR;
+    p.n_kt = (b.Sk + TR - 1) / TR;
+    p.causal = b.causal;
+    p.scale = b.scale;
+    p.scale_log2 = b.scale * LOG2E;
+    p.cap_in = b.softcap > 0.f ? b.scale / b.softcap : 0.f;
+    p.cap_out = b.softcap * LOG2E;
+
+    // row intervals and tile summaries
+    bwd_rows_kernel<<<dim3(p.n_qt, b.B), TR, 0, stream>>>(reinterpret_cast<const int2*>(b.row_bounds),
+                                                          reinterpret_cast<int2*>(b.ws_rows),
+                                                          reinterpret_cast<int4*>(b.ws_summ), b.Sq, b.Sk, p.Sq_pad,
+                                                          p.n_qt, b.causal, b.wl, b.wr);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // Delta and base-2 lse
+    const long long n_rows = (long long)b.B * b.Hq * p.Sq_pad;
+    long long blocks = (n_rows * 32 + 255) / 256;
+    const long long cap_blocks = (long long)b.num_sms * 16;
+    if (blocks > cap_blocks) blocks = cap_blocks;
+    const uint16_t* dO = static_cast<const uint16_t*>(b.dout);
+    const uint16_t* O = static_cast<const uint16_t*>(b.out);
+    if (b.D == 128) {
+        if (b.f16)
+            bwd_delta_kernel<128, true><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
+                                                                         b.Sq, p.Sq_pad);
+        else
+            bwd_delta_kernel<128, false><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
+                                                                          b.Sq, p.Sq_pad);
+    } else {
+        if (b.f16)
+            bwd_delta_kernel<64, true><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
+                                                                        b.Sq, p.Sq_pad);
+        else
+            bwd_delta_kernel<64, false><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
+                                                                         b.Sq, p.Sq_pad);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    const int items_a = p.n_kt * b.B * b.Hkv, items_b = p.n_qt * b.B * b.Hq;
+    const int grid_a = items_a < b.num_sms ? items_a : b.num_sms;
+    const int grid_b = items_b < b.num_sms ? items_b : b.num_sms;
+    const bool cap = b.softcap > 0.f, ali = b.slopes != nullptr;
+    if (b.D == 128)
+        return b.f16 ? launch_flags<128, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream)
+                     : launch_flags<128, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream);
+    return b.f16 ? launch_flags<64, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream)
+                 : launch_flags<64, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream);
+}
+
+}  // namespace gbattn

@@ -61,6 +61,36 @@ struct DecodeProblem {
     int max_blocks, block_size, num_blocks;
 };
 
+// A validated backward problem.  The forward's out and lse are given or were
+// recomputed into the workspace before the launch.
+struct BwdProblem {
+    const void* q;
+    const void* k;
+    const void* v;
+    const void* out;            // [B, Hq, Sq, D]
+    const float* lse;           // [B, Hq, Sq]
+    const void* dout;           // [B, Hq, Sq, D]
+    const float* slopes;        // [Hq] or nullptr
+    const int32_t* row_bounds;  // [B, Sq, 2] or nullptr
+    void* dq;                   // [B, Hq, Sq, D]
+    void* dk;                   // [B, Hkv, Sk, D]
+    void* dv;                   // [B, Hkv, Sk, D]
+    int B, Hq, Hkv, Sq, Sk, D;
+    float scale;
+    int causal;
+    int wl, wr;
+    float softcap;
+    int f16;
+    // workspace regions (Sq_pad = Sq rounded up to 128)
+    float* ws_lse2;             // [B * Hq * Sq_pad]
+    float* ws_delta;            // [B * Hq * Sq_pad]
+    int32_t* ws_rows;           // [B * Sq_pad * 2]
+    int32_t* ws_summ;           // [B * ceil(Sq / 128) * 4]
+    unsigned int* status;
+    unsigned long long timeout_ns;
+    int num_sms;
+};
+
 // Bits of the device status word: which wait gave up.
 enum : unsigned int {
     ST_PREFILL_PRODUCER = 1u << 0,
@@ -71,6 +101,9 @@ enum : unsigned int {
     ST_DECODE_PRODUCER = 1u << 8,
     ST_DECODE_CONSUMER = 1u << 9,
     ST_DECODE_PAGED_RANGE = 1u << 10,  // a physical block index >= num_blocks, or a context past the table
+    ST_BWD_PRODUCER = 1u << 12,
+    ST_BWD_MMA = 1u << 13,
+    ST_BWD_EW = 1u << 14,
     ST_DIAG = 1u << 16,
 };
 
@@ -92,6 +125,11 @@ cudaError_t launch_prefill_bf16(const FwdProblem& p, const CUtensorMap& tq, cons
 cudaError_t launch_prefill_f32(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream);
+
+cudaError_t launch_backward_bf16(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tdo,
+                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
+// Rows of the backward's per-row workspace arrays: Sq rounded up to 128.
+size_t backward_sq_pad(int Sq);
 
 // Device address of the library's status word and the SM count of the current
 // device (looked up once per device).  False if the CUDA runtime fails.
