@@ -11,7 +11,9 @@ A step is one pass of the hot path over one batch of synthetic input:
     with seeded contexts of 4096..8192 keys in 64-token blocks of a shuffled
     pool;
   * varlen prefill (reported beside it): attn_fwd_varlen on 32 packed causal
-    sequences of seeded lengths 512..4096.
+    sequences of seeded lengths 512..4096;
+  * backward (reported beside it): attn_bwd on the headline shape with the
+    forward's out and lse given (dQ, dK, dV; 10 D flops per admissible pair).
 value = causal-adjusted attention TFLOP/s (4 D flops per admissible
 (query, key) pair) over all ranks.  The decode object reports HBM GB/s of its
 algorithmic bytes (Q + K + V + O).
@@ -61,7 +63,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time of the CPU baseline")
     ap.add_argument("--no-paged", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "decode", "both", "paged", "varlen"], default=None,
+    ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode", "both", "paged", "varlen", "backward"], default=None,
                     help="launch warm-up + steps of one path and exit (for ncu); no timing, one input copy")
     ap.add_argument("--decode-b", type=int, default=None, help="override the decode batch (smaller ncu captures)")
     return ap.parse_args()
@@ -167,6 +170,7 @@ def max_over_ranks(x: float, ws: int) -> float:
 KERNEL_SOURCES = {
     "prefill": ("prefill_bf16.cu", "ptx.cuh", "kernels.h"),
     "decode": ("decode_bf16.cu", "ptx.cuh", "kernels.h"),
+    "backward": ("backward_bf16.cu", "ptx.cuh", "kernels.h"),
 }
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch
@@ -442,6 +446,73 @@ def bench_varlen(g, args, ws, dev, pk):
                          "peak_source": f"bf16_tflops ({pk['source']}, burst)"}}
 
 
+BWD_SHAPE = dict(B=4, Hq=32, Hkv=8, S=2048, D=128)
+
+
+def bwd_workload_name():
+    c = BWD_SHAPE
+    return f"bf16_causal_bwd_b{c['B']}_h{c['Hq']}_kv{c['Hkv']}_s{c['S']}_d{c['D']}"
+
+
+def bench_backward(g, args, ws, dev, pk):
+    """Attention backward (attn_bwd with the forward's out and lse given, as
+    in training) on the headline shape: bf16 causal B4 Hq32 Hkv8 S2048 D128.
+    value = TFLOP/s of 10 D flops per admissible (query, key) pair (the five
+    products S, dP, dV, dK, dQ); the kernels run seven (S and dP are formed
+    once in each of the two main kernels).  Inputs (q, k, v, dO, out: 224 MiB)
+    exceed L2."""
+    import synth
+    c = BWD_SHAPE
+    B, Hq, Hkv, S, D = c["B"], c["Hq"], c["Hkv"], c["S"], c["D"]
+    q = synth.normal((B, Hq, S, D), 0, synth.STREAM_Q, torch.bfloat16, dev)
+    k = synth.normal((B, Hkv, S, D), 0, synth.STREAM_K, torch.bfloat16, dev)
+    v = synth.normal((B, Hkv, S, D), 0, synth.STREAM_V, torch.bfloat16, dev)
+    do = synth.normal((B, Hq, S, D), 0, synth.STREAM_DO, torch.bfloat16, dev)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+    out = g.attn_fwd(q, k, v, causal=True, lse=lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsb = torch.empty(g.bwd_workspace_size(B, Hq, Hkv, S, S, D, recompute=False), dtype=torch.uint8, device=dev)
+    fn = lambda i: g.attn_bwd(q, k, v, do, out, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=wsb)
+    for i in range(args.warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    if g.device_status() != 0:
+        raise RuntimeError("device status word set during the backward warm-up")
+    if args.profile:
+        for i in range(args.steps):
+            fn(i)
+        torch.cuda.synchronize()
+        return None
+    soak(fn, 0.5)
+    stream = torch.cuda.current_stream()
+    ms = max_over_ranks(time_region(fn, args.steps, ws, stream), ws)
+    per = ms / args.steps
+    pairs = B * Hq * S * (S + 1) / 2
+    flops = 10.0 * D * pairs
+    tf = flops / (per * 1e-3) / 1e12
+    # per-launch durations from CUDA events recorded between the launches
+    *_, phases = g.attn_bwd(q, k, v, do, out, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=wsb,
+                            phase_times_reps=args.steps)
+    _, prep_ms, dkdv_ms, dq_ms = phases
+    tf_a = 8.0 * D * pairs / (dkdv_ms * 1e-3) / 1e12  # S, dP, dV, dK
+    tf_b = 6.0 * D * pairs / (dq_ms * 1e-3) / 1e12    # S, dP, dQ
+    name = bwd_workload_name()
+    return {"workload": name, "metric": "attention backward TFLOP/s (causal-adj, 10 D flops per admissible pair)",
+            "value": round(tf * ws, 2), "unit": "TFLOP/s", "ms_per_step": round(per, 4), "flops_per_step": flops,
+            "flops_convention": "5 products x 2 D per admissible pair; the pages' cost line counts 12 D "
+                                "(a 4 D forward recompute)",
+            "gpu_launches": 4 * args.steps,
+            "phase_ms": {"prep": round(prep_ms, 4), "dkdv": round(dkdv_ms, 4), "dq": round(dq_ms, 4)},
+            "roofline": {"bound": "tensor", "kernel": "bwd_kernel dK/dV (S, dP, dV, dK: 8 D flops per pair)",
+                         "achieved": round(tf_a, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": round(tf_a / pk["bf16"], 4), "traffic": ncu_traffic("backward", name + ":dkdv"),
+                         "peak_source": f"bf16_tflops ({pk['source']}, burst)"},
+            "roofline_dq": {"bound": "tensor", "kernel": "bwd_kernel dQ (S, dP, dQ: 6 D flops per pair)",
+                            "achieved": round(tf_b, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
+                            "frac": round(tf_b / pk["bf16"], 4), "traffic": ncu_traffic("backward", name + ":dq"),
+                            "peak_source": f"bf16_tflops ({pk['source']}, burst)"}}
+
+
 def decode_graph_timing(fn, args, ws, stream, per_graph=10):
     """The decode step replayed from a CUDA graph of `per_graph` steps (the
     same calls, so host launch overhead is the only difference from eager)."""
@@ -553,6 +624,8 @@ def main():
             bench_decode_paged(g, args, ws, dev, pk)
         if args.profile == "varlen":
             bench_varlen(g, args, ws, dev, pk)
+        if args.profile == "backward":
+            bench_backward(g, args, ws, dev, pk)
         if g.device_status() != 0:
             raise RuntimeError("device status word set")
         if rank == 0:
@@ -565,6 +638,7 @@ def main():
         dec = None if args.no_decode else bench_decode(g, args, ws, dev, pk)
         paged = None if args.no_paged else bench_decode_paged(g, args, ws, dev, pk)
         varl = None if args.no_varlen else bench_varlen(g, args, ws, dev, pk)
+        bwd = None if args.no_backward else bench_backward(g, args, ws, dev, pk)
     finally:
         clocks = sampler.stop()
     if g.device_status() != 0:
@@ -592,6 +666,8 @@ def main():
         line["decode_paged"] = paged
     if varl is not None:
         line["varlen"] = varl
+    if bwd is not None:
+        line["backward"] = bwd
     if rank == 0 and not args.no_cpu_baseline:
         x_cpu = make_inputs(w, "cpu")
         tf, sample, threads = oracle_sample(w, x_cpu, args.cpu_seconds)

@@ -304,6 +304,17 @@ typedef struct {
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int recompute);
 int attn_bwd(const gbattn_bwd_params* p);
 
+/*
+ * attn_bwd_phase_times -- profiling form of attn_bwd: runs it `reps` times
+ * (1 .. 100000) with CUDA events recorded on p->stream between its launches,
+ * waits for each run, and writes the mean milliseconds of its four phases to
+ * phase_ms[4]: the forward recompute (0 when out and lse are given), the prep
+ * launches (row intervals, Delta), the dK / dV launch and the dQ launch.  The
+ * gradients are written as by attn_bwd.  Synchronous; creates and destroys its
+ * own events.
+ */
+int attn_bwd_phase_times(const gbattn_bwd_params* p, int reps, float* phase_ms);
+
 /* Human-readable text of a status code (static storage). */
 const char* gbattn_status_string(int status);
 

@@ -98,6 +98,8 @@ def lib() -> ctypes.CDLL:
             L.attn_bwd_workspace_size.restype = Z
             L.attn_bwd.argtypes = [ctypes.POINTER(_BwdParams)]
             L.attn_bwd.restype = I
+            L.attn_bwd_phase_times.argtypes = [ctypes.POINTER(_BwdParams), I, ctypes.POINTER(ctypes.c_float)]
+            L.attn_bwd_phase_times.restype = I
             L.gbattn_status_string.argtypes = [I]
             L.gbattn_status_string.restype = ctypes.c_char_p
             L.gbattn_device_status.argtypes = [P, I]
@@ -335,7 +337,7 @@ def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, recompute=True) -> int:
 
 def attn_bwd(q, k, v, dout, out=None, lse=None, alibi_slopes=None, *, softmax_scale=None, causal=False,
              window_left=None, window_right=None, softcap=None, row_kv_bounds=None, dq=None, dk=None, dv=None,
-             workspace=None, stream=None):
+             workspace=None, stream=None, phase_times_reps=0):
     """Attention backward by recompute.  q, dout [B,Hq,Sq,D], k/v [B,Hkv,Sk,D]
     (bf16 or fp16, CUDA); the forward's flags.
 
@@ -344,6 +346,9 @@ def attn_bwd(q, k, v, dout, out=None, lse=None, alibi_slopes=None, *, softmax_sc
     the workspace.  workspace: optional uint8 CUDA tensor of at least
     bwd_workspace_size(...) bytes, allocated here (through torch) when None.
     Returns (dq [B,Hq,Sq,D], dk [B,Hkv,Sk,D], dv [B,Hkv,Sk,D]) of q's dtype.
+    With phase_times_reps = n > 0 the call is the synchronous profiling form
+    (attn_bwd_phase_times): it runs n times and returns, after the gradients,
+    the mean milliseconds of (forward recompute, prep, dK/dV, dQ).
     """
     if q.dtype not in _DT16:
         raise TypeError(f"attn_bwd takes bf16 or fp16, got {q.dtype}")
@@ -386,6 +391,12 @@ def attn_bwd(q, k, v, dout, out=None, lse=None, alibi_slopes=None, *, softmax_sc
                      B, Hq, Hkv, Sq, Sk, D, scale, int(bool(causal)), _win(window_left), _win(window_right),
                      float(softcap or 0.0), _DT[q.dtype], workspace.data_ptr(), workspace.numel(),
                      _stream_handle(stream).value)
+    if phase_times_reps:
+        ms = (ctypes.c_float * 4)()
+        st = lib().attn_bwd_phase_times(ctypes.byref(prm), int(phase_times_reps), ms)
+        if st:
+            raise GbattnError(st, "attn_bwd_phase_times")
+        return dq, dk, dv, tuple(float(x) for x in ms)
     st = lib().attn_bwd(ctypes.byref(prm))
     if st:
         raise GbattnError(st, "attn_bwd")

@@ -342,7 +342,9 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, in
     return bwd_layout(B, Hq, Sq, D, recompute != 0).total;
 }
 
-int attn_bwd(const gbattn_bwd_params* a) {
+// attn_bwd, with optional events (5): before the forward recompute, then
+// those of launch_backward_bf16.
+static int bwd_run(const gbattn_bwd_params* a, cudaEvent_t* ev) {
     if (!a) return GBATTN_ERR_INVALID_ARG;
     int rc = check_common(a->B, a->Hq, a->Hkv, a->Sq, a->Sk, a->D, a->softmax_scale, a->softcap, a->dtype);
     if (rc) return rc;
@@ -382,6 +384,7 @@ int attn_bwd(const gbattn_bwd_params* a) {
     uint8_t* ws = static_cast<uint8_t*>(a->workspace);
     const void* out = a->out;
     const float* lse = a->lse;
+    if (ev && cudaEventRecord(ev[0], static_cast<cudaStream_t>(a->stream)) != cudaSuccess) return GBATTN_ERR_CUDA;
     if (rec) {
         // recompute the forward's output and lse into the workspace
         gbattn_fwd_params f{};
@@ -445,8 +448,36 @@ int attn_bwd(const gbattn_bwd_params* a) {
         !cached_map(&tk, a->k, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h) ||
         !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h))
         return GBATTN_ERR_CUDA;
-    cudaError_t e = launch_backward_bf16(b, tq, tdo, tk, tv, static_cast<cudaStream_t>(a->stream));
+    cudaError_t e = launch_backward_bf16(b, tq, tdo, tk, tv, static_cast<cudaStream_t>(a->stream),
+                                         ev ? ev + 1 : nullptr);
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+}
+
+int attn_bwd(const gbattn_bwd_params* a) { return bwd_run(a, nullptr); }
+
+int attn_bwd_phase_times(const gbattn_bwd_params* a, int reps, float* phase_ms) {
+    if (!a || !phase_ms || reps <= 0 || reps > 100000) return GBATTN_ERR_INVALID_ARG;
+    cudaEvent_t ev[5] = {};
+    for (int i = 0; i < 5; ++i)
+        if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(ev[j]);
+            return GBATTN_ERR_CUDA;
+        }
+    double acc[4] = {0, 0, 0, 0};
+    int rc = GBATTN_OK;
+    for (int r = 0; r < reps && rc == GBATTN_OK; ++r) {
+        rc = bwd_run(a, ev);
+        if (rc == GBATTN_OK && cudaEventSynchronize(ev[4]) != cudaSuccess) rc = GBATTN_ERR_CUDA;
+        for (int i = 0; i < 4 && rc == GBATTN_OK; ++i) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, ev[i], ev[i + 1]) != cudaSuccess) rc = GBATTN_ERR_CUDA;
+            acc[i] += ms;
+        }
+    }
+    for (int i = 0; i < 5; ++i) cudaEventDestroy(ev[i]);
+    if (rc == GBATTN_OK)
+        for (int i = 0; i < 4; ++i) phase_ms[i] = (float)(acc[i] / reps);
+    return rc;
 }
 
 static int decode_plan(int B, int Hq, int Hkv, int Sk, int D, int num_splits, int* splits, int* chunk) {

@@ -53,6 +53,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -161,39 +163,44 @@ __global__ void __launch_bounds__(TR) bwd_rows_kernel(const int2* __restrict__ r
 }
 
 // ---------------------------------------------------------------------------- Delta and base-2 lse
-// One warp per padded row (b h, i): Delta = dO . O in fp32, lse2 = lse * log2(e).
+// Per padded row (b h, i): Delta = dO . O in fp32, lse2 = lse * log2(e).  A
+// row is D / 8 lanes with one 16-byte load of dO and of O each, so a warp
+// takes 32 / (D / 8) rows per pass.
 template <int D, bool F16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ dout,
                                                         const uint16_t* __restrict__ out,
                                                         const float* __restrict__ lse, float* __restrict__ lse2,
                                                         float* __restrict__ delta, long long n_rows, int Sq,
                                                         int Sq_pad) {
-    constexpr int PER = D / 32;  // elements per lane
-    const int lane = threadIdx.x & 31;
+    constexpr int LPR = D / 8;     // lanes per row
+    constexpr int RPW = 32 / LPR;  // rows per warp and pass
+    const int lane = threadIdx.x & 31, sub = lane / LPR, l = lane % LPR;
     const long long w0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    for (long long row = w0; row < n_rows; row += nw) {
-        const long long bh = row / Sq_pad;
-        const int i = (int)(row - bh * Sq_pad);
+    for (long long base = w0 * RPW; base < n_rows; base += nw * RPW) {
+        const long long row = base + sub;
         float d = 0.f, l2 = INFINITY;
-        if (i < Sq) {
-            const size_t off = ((size_t)bh * Sq + i) * D + lane * PER;
-            uint16_t a[PER], c[PER];
-            if (PER == 4) {
-                *reinterpret_cast<uint2*>(a) = *reinterpret_cast<const uint2*>(dout + off);
-                *reinterpret_cast<uint2*>(c) = *reinterpret_cast<const uint2*>(out + off);
-            } else {
-                *reinterpret_cast<uint32_t*>(a) = *reinterpret_cast<const uint32_t*>(dout + off);
-                *reinterpret_cast<uint32_t*>(c) = *reinterpret_cast<const uint32_t*>(out + off);
+        if (row < n_rows) {
+            const long long bh = row / Sq_pad;
+            const int i = (int)(row - bh * Sq_pad);
+            if (i < Sq) {
+                const size_t off = ((size_t)bh * Sq + i) * D + l * 8;
+                const uint4 a = *reinterpret_cast<const uint4*>(dout + off);
+                const uint4 c = *reinterpret_cast<const uint4*>(out + off);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    d = fmaf(widen16<F16>((uint16_t)(aw[t] & 0xffffu)), widen16<F16>((uint16_t)(cw[t] & 0xffffu)), d);
+                    d = fmaf(widen16<F16>((uint16_t)(aw[t] >> 16)), widen16<F16>((uint16_t)(cw[t] >> 16)), d);
+                }
+                const float lv = lse[(size_t)bh * Sq + i];
+                l2 = (lv == -INFINITY) ? INFINITY : lv * LOG2E;
             }
-#pragma unroll
-            for (int t = 0; t < PER; ++t) d = fmaf(widen16<F16>(a[t]), widen16<F16>(c[t]), d);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            const float l = lse[(size_t)bh * Sq + i];
-            l2 = (l == -INFINITY) ? INFINITY : l * LOG2E;
         }
-        if (lane == 0) {
+        // sum over the row's lanes (every lane takes part)
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        if (row < n_rows && l == 0) {
             lse2[row] = l2;
             delta[row] = d;
         }
@@ -374,6 +381,8 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
             }
             w = w && mbar_wait(&sm.s_full, step & 1u, wc, ST_BWD_EW);
             if (!__all_sync(0xffffffffu, w)) return false;
+            // DQ = 0: does any lane of the warp have a masked column?
+            const bool warp_masked = !DQ && __any_sync(0xffffffffu, adm != ~0ull);
             tc_fence_after();
             float sv[64];
             tmem_ld64(tS, sv);
@@ -389,26 +398,39 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
                 const float* xl = reinterpret_cast<const float*>(sX + st * EXTRA_BYTES) + c0;  // lse2
                 const int kj = it.t * TR + r;
                 const float abase = ALIBI ? slope_l2 * (float)(kj - u * TR - c0) : 0.f;
+                const uint32_t adm_lo = (uint32_t)adm, adm_hi = (uint32_t)(adm >> 32);
+                // the column loop, with or without the per-column mask (a warp-uniform choice)
+                auto p_loop = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    float z[2], f[2] = {1.f, 1.f};
+                    for (int c = 0; c < 64; c += 2) {
+                        float z[2], f[2] = {1.f, 1.f};
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        if (SOFTCAP) {
-                            const float t = tanh_approx(sv[c + e] * p.cap_in);
-                            z[e] = p.cap_out * t;
-                            f[e] = fmaf(-t, t, 1.f);
-                        } else {
-                            z[e] = sv[c + e] * p.scale_log2;
+                        for (int e = 0; e < 2; ++e) {
+                            const int cc = c + e;
+                            if (SOFTCAP) {
+                                const float t = tanh_approx(sv[cc] * p.cap_in);
+                                z[e] = fmaf(p.cap_out, t, -xl[cc]);
+                                f[e] = fmaf(-t, t, 1.f);
+                            } else {
+                                z[e] = fmaf(sv[cc], p.scale_log2, -xl[cc]);
+                            }
+                            if (ALIBI) z[e] += fmaf(-slope_l2, (float)cc, abase);
+                            float pe = ex2_approx(z[e]);
+                            if (decltype(masked)::value) {
+                                const uint32_t word = cc < 32 ? adm_lo : adm_hi;
+                                pe = ((int)(word << (31 - (cc & 31))) < 0) ? pe : 0.f;
+                            }
+                            z[e] = pe;
                         }
-                        if (ALIBI) z[e] += fmaf(-slope_l2, (float)(c + e), abase);
-                        const float pe = ex2_approx(z[e] - xl[c + e]);
-                        z[e] = ((adm >> (c + e)) & 1ull) ? pe : 0.f;
+                        pw[c >> 1] = pack16x2<F16>(z[0], z[1]);
+                        sv[c] = z[0] * f[0];
+                        sv[c + 1] = z[1] * f[1];
                     }
-                    pw[c >> 1] = pack16x2<F16>(z[0], z[1]);
-                    sv[c] = z[0] * f[0];
-                    sv[c + 1] = z[1] * f[1];
-                }
+                };
+                if (warp_masked)
+                    p_loop(std::true_type{});
+                else
+                    p_loop(std::false_type{});
                 tmem_st32(tS, pw);
                 tmem_wait_st();
                 tc_fence_before();
@@ -418,23 +440,30 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
                 const int i = it.t * TR + r;
                 const int kb = u * TR + c0;
                 const int lo = ra - kb, hi = rb - kb;
-                const bool need = kb < ra || kb + 63 > rb;
+                // the vote is taken by the converged warp, outside any per-lane branch
+                const bool need = __any_sync(0xffffffffu, kb < ra || kb + 63 > rb);
                 const float abase = ALIBI ? slope_l2 * (float)(kb - i) : 0.f;
+                auto p_loop = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    float z, f = 1.f;
-                    if (SOFTCAP) {
-                        const float t = tanh_approx(sv[c] * p.cap_in);
-                        z = p.cap_out * t;
-                        f = fmaf(-t, t, 1.f);
-                    } else {
-                        z = sv[c] * p.scale_log2;
+                    for (int c = 0; c < 64; ++c) {
+                        float z, f = 1.f;
+                        if (SOFTCAP) {
+                            const float t = tanh_approx(sv[c] * p.cap_in);
+                            z = fmaf(p.cap_out, t, -lse2_i);
+                            f = fmaf(-t, t, 1.f);
+                        } else {
+                            z = fmaf(sv[c], p.scale_log2, -lse2_i);
+                        }
+                        if (ALIBI) z += fmaf(slope_l2, (float)c, abase);
+                        float pe = ex2_approx(z);
+                        if (decltype(masked)::value) pe = (c < lo || c > hi) ? 0.f : pe;
+                        sv[c] = pe * f;
                     }
-                    if (ALIBI) z += fmaf(slope_l2, (float)c, abase);
-                    float pe = ex2_approx(z - lse2_i);
-                    if (need) pe = (c < lo || c > hi) ? 0.f : pe;
-                    sv[c] = pe * f;
-                }
+                };
+                if (need)
+                    p_loop(std::true_type{});
+                else
+                    p_loop(std::false_type{});
             }
             w = mbar_wait(&sm.dp_full, step & 1u, wc, ST_BWD_EW);
             if (!__all_sync(0xffffffffu, w)) return false;
@@ -735,7 +764,8 @@ cudaError_t launch_main(const BParams& prm, int grid, const CUtensorMap& tq, con
 
 template <int D, bool F16>
 cudaError_t launch_flags(const BParams& prm, int grid_a, int grid_b, bool cap, bool ali, const CUtensorMap& tq,
-                         const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream,
+                         cudaEvent_t* ev) {
     BParams pa = prm, pb = prm;
     pa.n_items = prm.n_kt * prm.B * prm.Hkv;
     pb.n_items = prm.n_qt * prm.B * prm.Hq;
@@ -743,7 +773,10 @@ cudaError_t launch_flags(const BParams& prm, int grid_a, int grid_b, bool cap, b
 #define GBATTN_BWD_PAIR(CAP, ALI)                                                              \
     e = launch_main<D, false, CAP, ALI, F16>(pa, grid_a, tq, tdo, tk, tv, stream);              \
     if (e != cudaSuccess) return e;                                                             \
-    return launch_main<D, true, CAP, ALI, F16>(pb, grid_b, tq, tdo, tk, tv, stream);
+    if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;                    \
+    e = launch_main<D, true, CAP, ALI, F16>(pb, grid_b, tq, tdo, tk, tv, stream);               \
+    if (e != cudaSuccess) return e;                                                             \
+    return ev ? cudaEventRecord(ev[3], stream) : cudaSuccess;
     if (cap) {
         if (ali) {
             GBATTN_BWD_PAIR(true, true)
@@ -765,7 +798,7 @@ cudaError_t launch_flags(const BParams& prm, int grid_a, int grid_b, bool cap, b
 size_t backward_sq_pad(int Sq) { return ((size_t)Sq + TR - 1) / TR * TR; }
 
 cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, const CUtensorMap& tdo,
-                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream, cudaEvent_t* ev) {
     BParams p{};
     p.dq = static_cast<uint16_t*>(b.dq);
     p.dk = static_cast<uint16_t*>(b.dk);
@@ -792,12 +825,14 @@ cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, con
     p.cap_in = b.softcap > 0.f ? b.scale / b.softcap : 0.f;
     p.cap_out = b.softcap * LOG2E;
 
+    cudaError_t e;
+    if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
     // row intervals and tile summaries
     bwd_rows_kernel<<<dim3(p.n_qt, b.B), TR, 0, stream>>>(reinterpret_cast<const int2*>(b.row_bounds),
                                                           reinterpret_cast<int2*>(b.ws_rows),
                                                           reinterpret_cast<int4*>(b.ws_summ), b.Sq, b.Sk, p.Sq_pad,
                                                           p.n_qt, b.causal, b.wl, b.wr);
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // Delta and base-2 lse
     const long long n_rows = (long long)b.B * b.Hq * p.Sq_pad;
@@ -823,16 +858,17 @@ cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, con
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
 
     const int items_a = p.n_kt * b.B * b.Hkv, items_b = p.n_qt * b.B * b.Hq;
     const int grid_a = items_a < b.num_sms ? items_a : b.num_sms;
     const int grid_b = items_b < b.num_sms ? items_b : b.num_sms;
     const bool cap = b.softcap > 0.f, ali = b.slopes != nullptr;
     if (b.D == 128)
-        return b.f16 ? launch_flags<128, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream)
-                     : launch_flags<128, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream);
-    return b.f16 ? launch_flags<64, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream)
-                 : launch_flags<64, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream);
+        return b.f16 ? launch_flags<128, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev)
+                     : launch_flags<128, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev);
+    return b.f16 ? launch_flags<64, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev)
+                 : launch_flags<64, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev);
 }
 
 }  // namespace gbattn

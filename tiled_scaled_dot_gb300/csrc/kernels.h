@@ -126,8 +126,11 @@ cudaError_t launch_prefill_f32(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream);
 
+// ev (optional, 4 events) is recorded before the prep launches, before the
+// dK / dV launch, before the dQ launch and after it.
 cudaError_t launch_backward_bf16(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream);
+                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream,
+                                 cudaEvent_t* ev = nullptr);
 // Rows of the backward's per-row workspace arrays: Sq rounded up to 128.
 size_t backward_sq_pad(int Sq);
 
