@@ -143,3 +143,25 @@ def test_bwd_full_size_sampled_groups(cuda_device):
         for name, got, want in zip(("dq", "dk", "dv"),
                                    (dq[b:b + 1, hs], dk[b:b + 1, kh:kh + 1], dv[b:b + 1, kh:kh + 1]), ref):
             check_grad(got, want, f"full size b{b} group{kh} {name}")
+
+
+def test_bwd_outputs_16_byte_aligned(cuda_device):
+    # gradient buffers 16 bytes past a 32-byte boundary take the 16-byte store
+    # path; the result is bitwise that of aligned buffers
+    import tiled_scaled_dot_gb300 as g
+    B, Hq, Hkv, S, D = 1, 4, 2, 200, 128
+    q, k, v, do = (t.to(cuda_device) for t in _inputs(B, Hq, Hkv, S, S, D, 10))
+
+    def offset_like(t):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=cuda_device)
+        out = buf[8:].view(t.shape)
+        assert out.data_ptr() % 32 == 16
+        return out
+
+    a = g.attn_bwd(q, k, v, do, causal=True)
+    dq, dk, dv = offset_like(q), offset_like(k), offset_like(v)
+    b = g.attn_bwd(q, k, v, do, causal=True, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)

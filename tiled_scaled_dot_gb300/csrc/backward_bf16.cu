@@ -26,8 +26,11 @@
 //                      dQ += dS K accumulated in TMEM.
 // The two main launches are one template: a pair of "fixed" tiles per item
 // (K, V or Q, dO) stays in shared memory while pairs of "streamed" tiles
-// (Q, dO or K, V) move through an NSTG-stage ring; both products S and dP take
-// the fixed tile as A (M = 128 lanes) and the streamed tile as B (N = 128).
+// (Q, dO or K, V) move one tile at a time through a ring of NSLOT shared-memory
+// slots (each with its own full and empty barrier, so a tile is released as
+// soon as its last reader has been issued and the next tiles land early);
+// both products S and dP take the fixed tile as A (M = 128 lanes) and the
+// streamed tile as B (N = 128).
 //
 // Structure (10 warps, one persistent CTA per SM):
 //   WG0, WG1 (warps 0-7)   element-wise: thread (g, r) owns TMEM lane r and
@@ -68,15 +71,19 @@ constexpr int EW_THREADS = 256;
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr int EXTRA_BYTES = 2048;  // per stage (DQ = 0): lse2[128], delta[128], rows int2[128]
+constexpr int EXTRA_BYTES = 2048;  // per T1 slot (DQ = 0): lse2[128], delta[128], rows int2[128]
+constexpr int MAX_SLOTS = 10;
 
-template <int D>
+template <int D, bool DQ>
 struct BCfg {
     static constexpr int HALVES = D / 64;
     static constexpr int TILE_BYTES = TR * D * 2;
     static constexpr int SLAB = TR * 128;  // one 64-column slab of a tile
-    static constexpr int NSTG = (D == 128) ? 2 : 4;
-    static constexpr int SMEM_BYTES = 2 * TILE_BYTES + NSTG * 2 * TILE_BYTES + NSTG * EXTRA_BYTES + 1024;
+    // streamed-tile slots: a step fills two (T1, then T2); as many as fit
+    // beside the fixed tiles in 227 KB
+    static constexpr int NSLOT = DQ ? (D == 128 ? 5 : 10) : (D == 128 ? 4 : 8);
+    static constexpr int SMEM_BYTES = 2 * TILE_BYTES + NSLOT * TILE_BYTES + (DQ ? 0 : NSLOT * EXTRA_BYTES) + 1024;
+    static_assert(NSLOT <= MAX_SLOTS && SMEM_BYTES <= 232448 - 512, "shared memory");
     static constexpr uint32_t ACC1 = 256;      // dV (DQ = 0) or dQ (DQ = 1)
     static constexpr uint32_t ACC2 = 256 + D;  // dK (DQ = 0)
 };
@@ -99,6 +106,7 @@ struct BParams {
     float cap_in;      // softmax_scale / softcap
     float cap_out;     // softcap * log2(e)
     int n_items;
+    int wide_store;    // dq, dk, dv are 32-byte aligned: 32-byte stores
 };
 
 __device__ __forceinline__ int item_of(int k, int cta, int grid) {
@@ -109,6 +117,21 @@ __device__ __forceinline__ float tanh_approx(float x) {
     float y;
     asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Fetch one box of a tensor map into L2 ahead of its TMA load.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// One 32-byte global store; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32b(void* p, const uint32_t* r) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 template <bool F16>
@@ -257,7 +280,7 @@ __device__ __forceinline__ void k_tile_range(const BParams& p, int b, int m, int
 
 struct BSmem {
     uint64_t fix_full, fix_empty;
-    uint64_t stg_full[4], stg_empty[4];
+    uint64_t slot_full[MAX_SLOTS], slot_empty[MAX_SLOTS];
     uint64_t s_full, dp_full, p_full, s_free, ds_full, acc_full, acc_empty;
     uint64_t drain;
     uint32_t tmem_base;
@@ -299,17 +322,20 @@ __device__ __forceinline__ int count_steps(const BParams& p, const BItem& it) {
 }
 
 // ---------------------------------------------------------------------------- element-wise role
-// Store 32 fp32 accumulator values (times f) of one output row as 16-bit.
+// Store 32 fp32 accumulator values (times f) of one output row as 16-bit:
+// two 32-byte stores when `wide` (dst 32-byte aligned), else four 16-byte ones.
 template <bool F16>
-__device__ __forceinline__ void store_row32(uint16_t* dst, const float (&v)[32], float f) {
+__device__ __forceinline__ void store_row32(uint16_t* dst, const float (&v)[32], float f, bool wide) {
+    uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint4 w;
-        w.x = pack16x2<F16>(v[8 * i + 0] * f, v[8 * i + 1] * f);
-        w.y = pack16x2<F16>(v[8 * i + 2] * f, v[8 * i + 3] * f);
-        w.z = pack16x2<F16>(v[8 * i + 4] * f, v[8 * i + 5] * f);
-        w.w = pack16x2<F16>(v[8 * i + 6] * f, v[8 * i + 7] * f);
-        reinterpret_cast<uint4*>(dst)[i] = w;
+    for (int i = 0; i < 16; ++i) w[i] = pack16x2<F16>(v[2 * i] * f, v[2 * i + 1] * f);
+    if (wide) {
+        st_global_32b(dst, w);
+        st_global_32b(dst + 16, w + 8);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
     }
 }
 
@@ -320,7 +346,7 @@ __device__ __forceinline__ void zero_row(uint16_t* dst, int n) {
 template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
 __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tmem, const WaitCtl& wc, int warp,
                                         const uint8_t* sX) {
-    using C = BCfg<D>;
+    using C = BCfg<D, DQ>;
     const int g = warp >> 2;          // column group: columns 64 g .. 64 g + 63
     const int r = threadIdx.x & (TR - 1);  // TMEM lane
     const int c0 = 64 * g;
@@ -357,15 +383,16 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
             delta_i = __ldg(p.delta + (size_t)(it.b * p.Hq + it.hd) * p.Sq_pad + i);
         }
         const bool ok = for_steps<DQ>(p, it, [&](int h, int u) -> bool {
-            const int st = (int)(stg % C::NSTG);
-            const uint32_t sp = (stg / C::NSTG) & 1u;
+            const uint32_t f1 = 2 * stg;  // fill index of the step's T1 tile (its extras sit beside it)
+            const int st = (int)(f1 % C::NSLOT);
+            const uint32_t sp = (f1 / C::NSLOT) & 1u;
             ++stg;
             bool w = true;
             // DQ = 0: admissible columns of this thread's key as a bit mask, from
             // the stage's row intervals (all ones when every row admits the tile)
             uint64_t adm = ~0ull;
             if (!DQ) {
-                w = mbar_wait(&sm.stg_full[st], sp, wc, ST_BWD_EW);
+                w = mbar_wait(&sm.slot_full[st], sp, wc, ST_BWD_EW);
                 const int k0 = it.t * TR, kj = k0 + r;
                 const int4 su = __ldg(p.summ + (size_t)it.b * p.n_qt + u);
                 if (w && !(su.z <= k0 && su.w >= k0 + TR - 1)) {
@@ -507,7 +534,7 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
             for (int c = 0; c < D / 2; c += 32) {
                 float v[32];
                 tmem_ld32(tmem + lane_off + C::ACC1 + g * (D / 2) + c, v);
-                if (i < p.Sq) store_row32<F16>(dst + c, v, p.scale);
+                if (i < p.Sq) store_row32<F16>(dst + c, v, p.scale, p.wide_store != 0);
             }
         } else {
             const int key = it.t * TR + r;
@@ -518,7 +545,7 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
             for (int c = 0; c < D; c += 32) {
                 float v[32];
                 tmem_ld32(tmem + lane_off + acc + c, v);
-                if (key < p.Sk) store_row32<F16>(dst + c, v, f);
+                if (key < p.Sk) store_row32<F16>(dst + c, v, f, p.wide_store != 0);
             }
         }
         tc_fence_before();
@@ -531,23 +558,23 @@ template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BParams p) {
-    using C = BCfg<D>;
+    using C = BCfg<D, DQ>;
     extern __shared__ __align__(1024) uint8_t dyn_smem[];
     __shared__ BSmem sm;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) & ~uintptr_t(1023));
     uint8_t* sF1 = base;                        // K (DQ = 0) or Q (DQ = 1)
     uint8_t* sF2 = base + C::TILE_BYTES;        // V or dO
-    uint8_t* sT = base + 2 * C::TILE_BYTES;     // stage s: T1 (Q or K) at 2 s, T2 (dO or V) at 2 s + 1 tiles
-    uint8_t* sX = sT + C::NSTG * 2 * C::TILE_BYTES;  // stage extras (DQ = 0)
+    uint8_t* sT = base + 2 * C::TILE_BYTES;     // streamed-tile slots
+    uint8_t* sX = sT + C::NSLOT * C::TILE_BYTES;  // per-slot extras (DQ = 0)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(&sm.fix_full, 1);
         mbar_init(&sm.fix_empty, 1);
-        for (int i = 0; i < C::NSTG; ++i) {
-            mbar_init(&sm.stg_full[i], 1);
-            mbar_init(&sm.stg_empty[i], 1);
+        for (int i = 0; i < C::NSLOT; ++i) {
+            mbar_init(&sm.slot_full[i], 1);
+            mbar_init(&sm.slot_empty[i], 1);
         }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.dp_full, 1);
@@ -579,17 +606,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_prefetch_desc(&tmDO);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
-            uint32_t fix_cnt = 0, stg = 0;
+            uint32_t fix_cnt = 0, fills = 0;  // fills: streamed tiles loaded so far (two per step)
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 const int item = item_of(k, cta, grid);
                 if (item >= p.n_items) break;
                 const BItem it = bwd_item<DQ>(p, item);
-                if (count_steps<DQ>(p, it) == 0) continue;
+                const int J = count_steps<DQ>(p, it);
+                if (J == 0) continue;
+                const int hkv = DQ ? it.hd / p.G : it.hd;
+                // Streamed tiles of the item's steps [lo, hi): T1 then T2 of each.
+                auto fill_steps = [&](int lo, int hi) -> bool {
+                    int j = 0;
+                    return for_steps<DQ>(p, it, [&](int h, int u) -> bool {
+                        const int jj = j++;
+                        if (jj < lo) return true;
+                        if (jj >= hi) return false;
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {  // x = 0: T1 (Q or K), x = 1: T2 (dO or V)
+                            const int sl = (int)(fills % C::NSLOT);
+                            if (!mbar_wait(&sm.slot_empty[sl], ((fills / C::NSLOT) & 1u) ^ 1u, wc, ST_BWD_PRODUCER))
+                                return ok = false;
+                            uint64_t* fb = &sm.slot_full[sl];
+                            const bool extras = !DQ && x == 0;
+                            mbar_arrive_expect_tx(fb, C::TILE_BYTES + (extras ? EXTRA_BYTES : 0));
+                            uint8_t* dst = sT + sl * C::TILE_BYTES;
+                            const CUtensorMap* m = DQ ? (x ? &tmV : &tmK) : (x ? &tmDO : &tmQ);
+                            const int plane = DQ ? it.b * p.Hkv + hkv : it.b * p.Hq + h;
+#pragma unroll
+                            for (int hf = 0; hf < C::HALVES; ++hf)
+                                tma_load_3d(dst + hf * C::SLAB, m, fb, hf * 64, u * TR, plane);
+                            if (extras) {
+                                const size_t row = (size_t)(it.b * p.Hq + h) * p.Sq_pad + (size_t)u * TR;
+                                uint8_t* xb = sX + sl * EXTRA_BYTES;
+                                bulk_load(xb, p.lse2 + row, 512, fb);
+                                bulk_load(xb + 512, p.delta + row, 512, fb);
+                                bulk_load(xb + 1024, p.rows + (size_t)it.b * p.Sq_pad + (size_t)u * TR, 1024, fb);
+                            }
+                            ++fills;
+                        }
+                        return true;
+                    });
+                };
+                // The first steps' tiles go out before the fixed tiles, which wait
+                // until the previous item's MMAs are done with theirs; the ring
+                // holds them, so this never waits on this item's own MMAs.
+                const int pre = J < C::NSLOT / 2 ? J : C::NSLOT / 2;
+                fill_steps(0, pre);
+                if (!ok) break;
                 ok = mbar_wait(&sm.fix_empty, (fix_cnt & 1u) ^ 1u, wc, ST_BWD_PRODUCER);
                 if (!ok) break;
                 mbar_arrive_expect_tx(&sm.fix_full, 2 * C::TILE_BYTES);
-                const int hkv = DQ ? it.hd / p.G : it.hd;
 #pragma unroll
                 for (int hf = 0; hf < C::HALVES; ++hf) {
                     if (DQ) {
@@ -601,39 +668,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 ++fix_cnt;
-                ok = for_steps<DQ>(p, it, [&](int h, int u) -> bool {
-                    const int st = (int)(stg % C::NSTG);
-                    if (!mbar_wait(&sm.stg_empty[st], ((stg / C::NSTG) & 1u) ^ 1u, wc, ST_BWD_PRODUCER)) return false;
-                    uint64_t* fb = &sm.stg_full[st];
-                    mbar_arrive_expect_tx(fb, 2 * C::TILE_BYTES + (DQ ? 0 : EXTRA_BYTES));
-                    uint8_t* t1 = sT + st * 2 * C::TILE_BYTES;
-                    uint8_t* t2 = t1 + C::TILE_BYTES;
+                {
+                    // the next item's fixed tiles, into L2 while this item runs
+                    const int nx = item_of(k + 1, cta, grid);
+                    if (nx < p.n_items) {
+                        const BItem in = bwd_item<DQ>(p, nx);
 #pragma unroll
-                    for (int hf = 0; hf < C::HALVES; ++hf) {
-                        if (DQ) {
-                            tma_load_3d(t1 + hf * C::SLAB, &tmK, fb, hf * 64, u * TR, it.b * p.Hkv + hkv);
-                            tma_load_3d(t2 + hf * C::SLAB, &tmV, fb, hf * 64, u * TR, it.b * p.Hkv + hkv);
-                        } else {
-                            tma_load_3d(t1 + hf * C::SLAB, &tmQ, fb, hf * 64, u * TR, it.b * p.Hq + h);
-                            tma_load_3d(t2 + hf * C::SLAB, &tmDO, fb, hf * 64, u * TR, it.b * p.Hq + h);
+                        for (int hf = 0; hf < C::HALVES; ++hf) {
+                            if (DQ) {
+                                tma_prefetch_l2_3d(&tmQ, hf * 64, in.t * TR, in.b * p.Hq + in.hd);
+                                tma_prefetch_l2_3d(&tmDO, hf * 64, in.t * TR, in.b * p.Hq + in.hd);
+                            } else {
+                                tma_prefetch_l2_3d(&tmK, hf * 64, in.t * TR, in.b * p.Hkv + in.hd);
+                                tma_prefetch_l2_3d(&tmV, hf * 64, in.t * TR, in.b * p.Hkv + in.hd);
+                            }
                         }
                     }
-                    if (!DQ) {
-                        const size_t row = (size_t)(it.b * p.Hq + h) * p.Sq_pad + (size_t)u * TR;
-                        uint8_t* x = sX + st * EXTRA_BYTES;
-                        bulk_load(x, p.lse2 + row, 512, fb);
-                        bulk_load(x + 512, p.delta + row, 512, fb);
-                        bulk_load(x + 1024, p.rows + (size_t)it.b * p.Sq_pad + (size_t)u * TR, 1024, fb);
-                    }
-                    ++stg;
-                    return true;
-                });
+                }
+                fill_steps(pre, J);
             }
             if (!ok) {
                 // let the copies already issued land before the CTA leaves
-                const uint32_t n = stg < (uint32_t)C::NSTG ? stg : (uint32_t)C::NSTG;
-                for (uint32_t i = stg - n; i < stg; ++i)
-                    mbar_drain(&sm.stg_full[i % C::NSTG], (i / C::NSTG) & 1u, 100000000ull);
+                const uint32_t n = fills < (uint32_t)C::NSLOT ? fills : (uint32_t)C::NSLOT;
+                for (uint32_t i = fills - n; i < fills; ++i)
+                    mbar_drain(&sm.slot_full[i % C::NSLOT], (i / C::NSLOT) & 1u, 100000000ull);
                 if (fix_cnt) mbar_drain(&sm.fix_full, (fix_cnt - 1) & 1u, 100000000ull);
             }
         }
@@ -647,8 +705,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr uint32_t IDESC_S = F16 ? idesc_f16_f32(TR, TR, 0) : idesc_bf16_f32(TR, TR, 0);
         constexpr uint32_t IDESC_A = F16 ? idesc_f16_f32(TR, D, 1) : idesc_bf16_f32(TR, D, 1);
         const uint32_t aF1 = smem_u32(sF1), aF2 = smem_u32(sF2), aT = smem_u32(sT);
-        auto t1_of = [&](uint32_t s) { return aT + (s % C::NSTG) * 2 * C::TILE_BYTES; };
-        auto t2_of = [&](uint32_t s) { return aT + (s % C::NSTG) * 2 * C::TILE_BYTES + C::TILE_BYTES; };
+        // streamed tile of fill index f: its slot address, its wait, its release
+        auto tile_of = [&](uint32_t f) { return aT + (f % C::NSLOT) * C::TILE_BYTES; };
+        auto wfill = [&](uint32_t f) { return wwait(&sm.slot_full[f % C::NSLOT], (f / C::NSLOT) & 1u); };
+        auto release = [&](uint32_t f) { umma_commit_elect(&sm.slot_empty[f % C::NSLOT]); };
         // D[col] = A B^T over K = D: both operands K-major 128 x D tiles
         auto mma_ss = [&](uint32_t col, uint32_t a, uint32_t b) {
             const uint32_t alo = sdesc_lo(a, 16), blo = sdesc_lo(b, 16);
@@ -678,54 +738,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (J == 0) continue;
             ok = wwait(&sm.fix_full, fix_cnt & 1u);
             ++fix_cnt;
-            ok = ok && wwait(&sm.stg_full[stg % C::NSTG], (stg / C::NSTG) & 1u);
+            const uint32_t f0 = 2 * stg;  // fills of step j: T1 = f0 + 2 j, T2 = f0 + 2 j + 1
+            ok = ok && wfill(f0);
             if (!ok) break;
             tc_fence_after();
-            mma_ss(0, aF1, t1_of(stg));
+            mma_ss(0, aF1, tile_of(f0));
             umma_commit_elect(&sm.s_full);
-            mma_ss(128, aF2, t2_of(stg));
+            if (!(ok = wfill(f0 + 1))) break;
+            tc_fence_after();
+            mma_ss(128, aF2, tile_of(f0 + 1));
             umma_commit_elect(&sm.dp_full);
+            if (DQ) release(f0 + 1);  // V_0 has no other reader
             for (int j = 0; j < J && ok; ++j, ++step) {
-                const uint32_t sj = stg + j, sn = sj + 1;
+                const uint32_t t1 = f0 + 2 * j, t2 = t1 + 1, n1 = t1 + 2, n2 = t1 + 3;
                 const bool more = j + 1 < J;
                 if (!DQ) {
                     ok = wwait(&sm.p_full, step & 1u);
                     if (ok && j == 0) ok = wwait(&sm.acc_empty, (acc_cnt & 1u) ^ 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    mma_ts(C::ACC1, 0, t2_of(sj), j > 0 ? 1u : 0u);  // dV += P^T dO
+                    mma_ts(C::ACC1, 0, tile_of(t2), j > 0 ? 1u : 0u);  // dV += P^T dO
+                    release(t2);                                        // dO_j: read by dP_j and dV_j
                     if (more) {
-                        if (!(ok = wwait(&sm.stg_full[sn % C::NSTG], (sn / C::NSTG) & 1u))) break;
+                        if (!(ok = wfill(n1))) break;
                         tc_fence_after();
-                        mma_ss(0, aF1, t1_of(sn));
+                        mma_ss(0, aF1, tile_of(n1));
                         umma_commit_elect(&sm.s_full);
                     }
                     if (!(ok = wwait(&sm.ds_full, step & 1u))) break;
                     tc_fence_after();
-                    mma_ts(C::ACC2, 128, t1_of(sj), j > 0 ? 1u : 0u);  // dK += dS^T Q
-                    umma_commit_elect(&sm.stg_empty[sj % C::NSTG]);
+                    mma_ts(C::ACC2, 128, tile_of(t1), j > 0 ? 1u : 0u);  // dK += dS^T Q
+                    release(t1);  // Q_j and its extras: read by S_j, dK_j and the element-wise warps
                     if (more) {
-                        mma_ss(128, aF2, t2_of(sn));
+                        if (!(ok = wfill(n2))) break;
+                        tc_fence_after();
+                        mma_ss(128, aF2, tile_of(n2));
                         umma_commit_elect(&sm.dp_full);
                     }
                 } else {
                     if (more) {
                         ok = wwait(&sm.s_free, step & 1u);
-                        ok = ok && wwait(&sm.stg_full[sn % C::NSTG], (sn / C::NSTG) & 1u);
+                        ok = ok && wfill(n1);
                         if (!ok) break;
                         tc_fence_after();
-                        mma_ss(0, aF1, t1_of(sn));
+                        mma_ss(0, aF1, tile_of(n1));
                         umma_commit_elect(&sm.s_full);
                     }
                     ok = wwait(&sm.ds_full, step & 1u);
                     if (ok && j == 0) ok = wwait(&sm.acc_empty, (acc_cnt & 1u) ^ 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    mma_ts(C::ACC1, 128, t1_of(sj), j > 0 ? 1u : 0u);  // dQ += dS K
-                    umma_commit_elect(&sm.stg_empty[sj % C::NSTG]);
+                    mma_ts(C::ACC1, 128, tile_of(t1), j > 0 ? 1u : 0u);  // dQ += dS K
+                    release(t1);                                          // K_j: read by S_j and dQ_j
                     if (more) {
-                        mma_ss(128, aF2, t2_of(sn));
+                        if (!(ok = wfill(n2))) break;
+                        tc_fence_after();
+                        mma_ss(128, aF2, tile_of(n2));
                         umma_commit_elect(&sm.dp_full);
+                        release(n2);  // V_{j+1}: read by dP_{j+1} only
                     }
                 }
             }
@@ -755,7 +825,7 @@ template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
 cudaError_t launch_main(const BParams& prm, int grid, const CUtensorMap& tq, const CUtensorMap& tdo,
                         const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
     auto kern = bwd_kernel<D, DQ, SOFTCAP, ALIBI, F16>;
-    const int smem = BCfg<D>::SMEM_BYTES;
+    const int smem = BCfg<D, DQ>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tdo, tk, tv, prm);
@@ -824,6 +894,8 @@ cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, con
     p.scale_log2 = b.scale * LOG2E;
     p.cap_in = b.softcap > 0.f ? b.scale / b.softcap : 0.f;
     p.cap_out = b.softcap * LOG2E;
+    p.wide_store = ((reinterpret_cast<uintptr_t>(b.dq) | reinterpret_cast<uintptr_t>(b.dk) |
+                     reinterpret_cast<uintptr_t>(b.dv)) & 31u) == 0;
 
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
