@@ -269,12 +269,13 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
  *  window_right, softcap   as in attn_fwd_ex.
  *  dq              device [B, Hq, Sq, D], written fully.
  *  dk, dv          device [B, Hkv, Sk, D], written fully.
- *  dtype           GBATTN_BF16 or GBATTN_F16 for every 16-bit tensor
- *                  (GBATTN_F32 returns GBATTN_ERR_UNSUPPORTED); D 64 or 128.
+ *  dtype           GBATTN_BF16 or GBATTN_F16 (tensor cores, fp32
+ *                  accumulation) or GBATTN_F32 (SIMT FFMA) for q, k, v, dout,
+ *                  out, dq, dk, dv alike; D 64 or 128.
  *  workspace       device, 256-byte aligned, at least
- *                  attn_bwd_workspace_size(...) bytes (recompute = 1 when out
- *                  and lse are NULL); the caller owns it; its contents are
- *                  scratch.
+ *                  attn_bwd_workspace_size(..., dtype, recompute) bytes
+ *                  (recompute = 1 when out and lse are NULL); the caller owns
+ *                  it; its contents are scratch.
  *  Errors: GBATTN_ERR_INVALID_ARG also for a gradient buffer that overlaps an
  *  input, another gradient or the workspace.
  */
@@ -301,7 +302,7 @@ typedef struct {
     void* stream;
 } gbattn_bwd_params;
 
-size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int recompute);
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int dtype, int recompute);
 int attn_bwd(const gbattn_bwd_params* p);
 
 /*

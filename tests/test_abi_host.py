@@ -162,10 +162,13 @@ def test_backward_rejects_bad_arguments(L):
     import tiled_scaled_dot_gb300 as g
     L.attn_bwd.argtypes = [ctypes.POINTER(g._BwdParams)]
     B, Hq, Hkv, S, D = 2, 4, 2, 256, 128
-    ws_need = L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 1)
-    ws_given = L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 0)
+    ws_need = L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 0, 1)
+    ws_given = L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 0, 0)
     assert ws_need > ws_given > 0
-    assert L.attn_bwd_workspace_size(B, 3, Hkv, S, S, D, 1) == 0  # Hq % Hkv
+    # the recomputed fp32 output takes twice the 16-bit one's bytes
+    assert L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 1, 1) - ws_given == 2 * (ws_need - ws_given) - B * Hq * S * 4
+    assert L.attn_bwd_workspace_size(B, 3, Hkv, S, S, D, 0, 1) == 0  # Hq % Hkv
+    assert L.attn_bwd_workspace_size(B, Hq, Hkv, S, S, D, 7, 1) == 0  # dtype
     nq, nkv = B * Hq * S * D * 2, B * Hkv * S * D * 2
     base = dict(q=FAKE, k=FAKE + nq, v=FAKE + nq + nkv, dout=FAKE + 2 * nq + 2 * nkv, dq=FAKE * 64,
                 dk=FAKE * 64 + nq, dv=FAKE * 64 + nq + nkv, B=B, Hq=Hq, Hkv=Hkv, Sq=S, Sk=S, D=D,
@@ -188,7 +191,7 @@ def test_backward_rejects_bad_arguments(L):
     assert call(causal=2) == 1
     assert call(window_left=-2) == 1
     assert call(D=96) == 2
-    assert call(dtype=1) == 2                            # fp32 backward not built
+    assert call(dtype=3) == 1                            # no such dtype
     assert call(dq=FAKE) == 1                            # dq aliasing q
     assert call(dv=FAKE * 64 + 8) == 1                   # dv overlapping dq (and misaligned)
     assert call(dk=FAKE * 128) == 1                      # dk inside the workspace

@@ -94,7 +94,7 @@ def lib() -> ctypes.CDLL:
             L.attn_decode_paged_workspace_size.restype = Z
             L.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, P, Z, I, P]
             L.attn_decode_paged.restype = I
-            L.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I]
+            L.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
             L.attn_bwd_workspace_size.restype = Z
             L.attn_bwd.argtypes = [ctypes.POINTER(_BwdParams)]
             L.attn_bwd.restype = I
@@ -331,15 +331,15 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slop
     return out
 
 
-def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, recompute=True) -> int:
-    return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, int(bool(recompute))))
+def bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, recompute=True, dtype=torch.bfloat16) -> int:
+    return int(lib().attn_bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, _DT[dtype], int(bool(recompute))))
 
 
 def attn_bwd(q, k, v, dout, out=None, lse=None, alibi_slopes=None, *, softmax_scale=None, causal=False,
              window_left=None, window_right=None, softcap=None, row_kv_bounds=None, dq=None, dk=None, dv=None,
              workspace=None, stream=None, phase_times_reps=0):
     """Attention backward by recompute.  q, dout [B,Hq,Sq,D], k/v [B,Hkv,Sk,D]
-    (bf16 or fp16, CUDA); the forward's flags.
+    (bf16, fp16 or fp32, CUDA); the forward's flags.
 
     out and lse: the forward's output and fp32 lse [B,Hq,Sq] (attn_fwd with
     lse=...), both or neither; when neither, the library recomputes them into
@@ -350,8 +350,8 @@ def attn_bwd(q, k, v, dout, out=None, lse=None, alibi_slopes=None, *, softmax_sc
     (attn_bwd_phase_times): it runs n times and returns, after the gradients,
     the mean milliseconds of (forward recompute, prep, dK/dV, dQ).
     """
-    if q.dtype not in _DT16:
-        raise TypeError(f"attn_bwd takes bf16 or fp16, got {q.dtype}")
+    if q.dtype not in _DT:
+        raise TypeError(f"attn_bwd takes bf16, fp16 or fp32, got {q.dtype}")
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
         _check(t, n, q.dtype, 4)
     B, Hq, Sq, D = q.shape
@@ -380,7 +380,7 @@ def attn_bwd(q, k, v, dout, out=None, lse=None, alibi_slopes=None, *, softmax_sc
         _check(t, n, q.dtype, 4)
         if t.shape != like.shape:
             raise ValueError(f"{n} must have the shape of its input")
-    need = bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, out is None)
+    need = bwd_workspace_size(B, Hq, Hkv, Sq, Sk, D, out is None, q.dtype)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     else:

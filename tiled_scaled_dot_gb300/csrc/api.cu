@@ -314,7 +314,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* 
 struct BwdLayout {
     size_t lse2, delta, rows, summ, lse, out, total;
 };
-static BwdLayout bwd_layout(int B, int Hq, int Sq, int D, bool recompute) {
+static BwdLayout bwd_layout(int B, int Hq, int Sq, int D, bool recompute, size_t esz) {
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t sp = backward_sq_pad(Sq), nqt = ((size_t)Sq + 127) / 128;
     BwdLayout L{};
@@ -331,15 +331,15 @@ static BwdLayout bwd_layout(int B, int Hq, int Sq, int D, bool recompute) {
         L.lse = o;
         o += up((size_t)B * Hq * Sq * 4);
         L.out = o;
-        o += up((size_t)B * Hq * Sq * D * 2);
+        o += up((size_t)B * Hq * Sq * D * esz);
     }
     L.total = o;
     return L;
 }
 
-size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int recompute) {
-    if (check_common(B, Hq, Hkv, Sq, Sk, D, 1.f, 0.f, GBATTN_BF16)) return 0;
-    return bwd_layout(B, Hq, Sq, D, recompute != 0).total;
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int Sq, int Sk, int D, int dtype, int recompute) {
+    if (check_common(B, Hq, Hkv, Sq, Sk, D, 1.f, 0.f, dtype)) return 0;
+    return bwd_layout(B, Hq, Sq, D, recompute != 0, dtype == GBATTN_F32 ? 4 : 2).total;
 }
 
 // attn_bwd, with optional events (5): before the forward recompute, then
@@ -348,7 +348,6 @@ static int bwd_run(const gbattn_bwd_params* a, cudaEvent_t* ev) {
     if (!a) return GBATTN_ERR_INVALID_ARG;
     int rc = check_common(a->B, a->Hq, a->Hkv, a->Sq, a->Sk, a->D, a->softmax_scale, a->softcap, a->dtype);
     if (rc) return rc;
-    if (a->dtype == GBATTN_F32) return GBATTN_ERR_UNSUPPORTED;
     if (a->B > 65535) return GBATTN_ERR_UNSUPPORTED;  // batch is a grid dimension of the row-interval launch
     if (!a->q || !a->k || !a->v || !a->dout || !a->dq || !a->dk || !a->dv || !a->workspace)
         return GBATTN_ERR_INVALID_ARG;
@@ -363,10 +362,11 @@ static int bwd_run(const gbattn_bwd_params* a, cudaEvent_t* ev) {
     if (a->lse && (reinterpret_cast<uintptr_t>(a->lse) & 3u)) return GBATTN_ERR_INVALID_ARG;
     if (a->alibi_slopes && (reinterpret_cast<uintptr_t>(a->alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
     const bool rec = a->out == nullptr;
-    const BwdLayout L = bwd_layout(a->B, a->Hq, a->Sq, a->D, rec);
+    const size_t esz = a->dtype == GBATTN_F32 ? 4 : 2;
+    const BwdLayout L = bwd_layout(a->B, a->Hq, a->Sq, a->D, rec, esz);
     if (a->workspace_bytes < L.total) return GBATTN_ERR_INVALID_ARG;
-    const size_t nq = (size_t)a->B * a->Hq * a->Sq * a->D * 2;
-    const size_t nkv = (size_t)a->B * a->Hkv * a->Sk * a->D * 2;
+    const size_t nq = (size_t)a->B * a->Hq * a->Sq * a->D * esz;
+    const size_t nkv = (size_t)a->B * a->Hkv * a->Sk * a->D * esz;
     const void* ins[5] = {a->q, a->k, a->v, a->dout, a->out};
     const size_t ins_n[5] = {nq, nkv, nkv, nq, nq};
     void* grads[3] = {a->dq, a->dk, a->dv};
@@ -441,6 +441,10 @@ static int bwd_run(const gbattn_bwd_params* a, cudaEvent_t* ev) {
     b.ws_rows = reinterpret_cast<int32_t*>(ws + L.rows);
     b.ws_summ = reinterpret_cast<int32_t*>(ws + L.summ);
     b.timeout_ns = g_timeout_ns;
+    if (a->dtype == GBATTN_F32) {
+        cudaError_t e = launch_backward_f32(b, static_cast<cudaStream_t>(a->stream), ev ? ev + 1 : nullptr);
+        return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
+    }
     const bool h = b.f16 != 0;
     CUtensorMap tq, tdo, tk, tv;
     if (!cached_map(&tq, a->q, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h) ||

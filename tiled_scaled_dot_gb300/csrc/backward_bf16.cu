@@ -867,6 +867,15 @@ cudaError_t launch_flags(const BParams& prm, int grid_a, int grid_b, bool cap, b
 
 size_t backward_sq_pad(int Sq) { return ((size_t)Sq + TR - 1) / TR * TR; }
 
+cudaError_t launch_backward_rows(const BwdProblem& b, cudaStream_t stream) {
+    const int Sq_pad = (int)backward_sq_pad(b.Sq), n_qt = (b.Sq + TR - 1) / TR;
+    bwd_rows_kernel<<<dim3(n_qt, b.B), TR, 0, stream>>>(reinterpret_cast<const int2*>(b.row_bounds),
+                                                        reinterpret_cast<int2*>(b.ws_rows),
+                                                        reinterpret_cast<int4*>(b.ws_summ), b.Sq, b.Sk, Sq_pad, n_qt,
+                                                        b.causal, b.wl, b.wr);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, const CUtensorMap& tdo,
                                  const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream, cudaEvent_t* ev) {
     BParams p{};
@@ -899,13 +908,7 @@ cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, con
 
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
-    // row intervals and tile summaries
-    bwd_rows_kernel<<<dim3(p.n_qt, b.B), TR, 0, stream>>>(reinterpret_cast<const int2*>(b.row_bounds),
-                                                          reinterpret_cast<int2*>(b.ws_rows),
-                                                          reinterpret_cast<int4*>(b.ws_summ), b.Sq, b.Sk, p.Sq_pad,
-                                                          p.n_qt, b.causal, b.wl, b.wr);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if ((e = launch_backward_rows(b, stream)) != cudaSuccess) return e;
     // Delta and base-2 lse
     const long long n_rows = (long long)b.B * b.Hq * p.Sq_pad;
     long long blocks = (n_rows * 32 + 255) / 256;

@@ -131,6 +131,11 @@ cudaError_t launch_decode_bf16(const DecodeProblem& p, const CUtensorMap& tk, co
 cudaError_t launch_backward_bf16(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tdo,
                                  const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream,
                                  cudaEvent_t* ev = nullptr);
+// The same for fp32 inputs (SIMT).
+cudaError_t launch_backward_f32(const BwdProblem& p, cudaStream_t stream, cudaEvent_t* ev = nullptr);
+// The backward's first launch (both storage types): each query row's admissible
+// key interval and the 128-row tile summaries, into the workspace.
+cudaError_t launch_backward_rows(const BwdProblem& p, cudaStream_t stream);
 // Rows of the backward's per-row workspace arrays: Sq rounded up to 128.
 size_t backward_sq_pad(int Sq);
 
