@@ -50,6 +50,8 @@
 //   [dS_j] dK += dS_j Q_j, dP_{j+1}
 // DQ = 1:
 //   S_0, dP_0, then per step j: [S_j read] S_{j+1}, [dS_j] dQ += dS_j K_j, dP_{j+1}
+// P and dS are handed over in two halves of each group's columns, each with
+// its own barrier; the MMAs reading a half go out as soon as it is in TMEM.
 // ([x] = wait for the element-wise warps).  tcgen05 operations issued by one
 // thread execute in order, so an MMA that overwrites a TMEM tile is issued
 // after the MMA that reads the tile's previous contents.
@@ -281,7 +283,8 @@ __device__ __forceinline__ void k_tile_range(const BParams& p, int b, int m, int
 struct BSmem {
     uint64_t fix_full, fix_empty;
     uint64_t slot_full[MAX_SLOTS], slot_empty[MAX_SLOTS];
-    uint64_t s_full, dp_full, p_full, s_free, ds_full, acc_full, acc_empty;
+    uint64_t s_full, dp_full, s_free, acc_full, acc_empty;
+    uint64_t p_half[2], ds_half[2];  // P / dS of columns 64 g + 32 h .. + 31 of both groups are in TMEM
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -322,6 +325,16 @@ __device__ __forceinline__ int count_steps(const BParams& p, const BItem& it) {
 }
 
 // ---------------------------------------------------------------------------- element-wise role
+// 32 lanes x 32 bits, 16 consecutive columns per thread (no wait).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 // Store 32 fp32 accumulator values (times f) of one output row as 16-bit:
 // two 32-byte stores when `wide` (dst 32-byte aligned), else four 16-byte ones.
 template <bool F16>
@@ -427,6 +440,11 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
                 const float abase = ALIBI ? slope_l2 * (float)(kj - u * TR - c0) : 0.f;
                 const uint32_t adm_lo = (uint32_t)adm, adm_hi = (uint32_t)(adm >> 32);
                 // the column loop, with or without the per-column mask (a warp-uniform choice)
+                // Each 32-column half is packed, stored and announced on its own,
+                // so the MMA warp starts dV on the first half while the second
+                // is computed.  Packed half h lands on columns 16 h .. 16 h + 15
+                // of the group's tile, which hold first-half S values already in
+                // registers.
                 auto p_loop = [&](auto masked) {
 #pragma unroll
                     for (int c = 0; c < 64; c += 2) {
@@ -452,16 +470,19 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
                         pw[c >> 1] = pack16x2<F16>(z[0], z[1]);
                         sv[c] = z[0] * f[0];
                         sv[c + 1] = z[1] * f[1];
+                        if (c == 30 || c == 62) {
+                            const int hf = c >> 5;
+                            tmem_st16(tS + 16 * hf, *reinterpret_cast<const uint32_t(*)[16]>(&pw[16 * hf]));
+                            tmem_wait_st();
+                            tc_fence_before();
+                            mbar_arrive(&sm.p_half[hf]);
+                        }
                     }
                 };
                 if (warp_masked)
                     p_loop(std::true_type{});
                 else
                     p_loop(std::false_type{});
-                tmem_st32(tS, pw);
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&sm.p_full);
             } else {
                 // thread = query row i, columns = keys k0 + c0 + c
                 const int i = it.t * TR + r;
@@ -495,8 +516,9 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
             w = mbar_wait(&sm.dp_full, step & 1u, wc, ST_BWD_EW);
             if (!__all_sync(0xffffffffu, w)) return false;
             tc_fence_after();
-            // dS in two 32-column halves (both read before the packed store
-            // overwrites the first half's columns)
+            // dS in two 32-column halves, each stored and announced on its own:
+            // packed half h goes to columns 16 h .. 16 h + 15 of the group's
+            // tile, which hold first-half dP values already read
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 float dp[32];
@@ -513,11 +535,11 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
                         pw[16 * hf + (c >> 1)] = pack16x2<F16>(sv[32 * hf + c] * (dp[c] - delta_i),
                                                                sv[32 * hf + c + 1] * (dp[c + 1] - delta_i));
                 }
+                tmem_st16(tDP + 16 * hf, *reinterpret_cast<const uint32_t(*)[16]>(&pw[16 * hf]));
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&sm.ds_half[hf]);
             }
-            tmem_st32(tDP, pw);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&sm.ds_full);
             ++step;
             return true;
         });
@@ -578,9 +600,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         mbar_init(&sm.s_full, 1);
         mbar_init(&sm.dp_full, 1);
-        mbar_init(&sm.p_full, EW_THREADS);
+        mbar_init(&sm.p_half[0], EW_THREADS);
+        mbar_init(&sm.p_half[1], EW_THREADS);
         mbar_init(&sm.s_free, EW_THREADS);
-        mbar_init(&sm.ds_full, EW_THREADS);
+        mbar_init(&sm.ds_half[0], EW_THREADS);
+        mbar_init(&sm.ds_half[1], EW_THREADS);
         mbar_init(&sm.acc_full, 1);
         mbar_init(&sm.acc_empty, EW_THREADS);
         mbar_init(&sm.drain, 1);
@@ -719,14 +743,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         };
         // D[col] (+)= A[TMEM, packed 16-bit at acol] B over K = 128 rows of the
-        // MN-major 128 x D tile b
-        auto mma_ts = [&](uint32_t col, uint32_t acol, uint32_t b, uint32_t acc) {
+        // MN-major 128 x D tile b, in two calls by half of the packed columns.
+        // The same for half hf of the packed columns: K chunks 2 hf, 2 hf + 1 of
+        // each group's 64 columns (P or dS handed over per half); the step's
+        // first MMA (half 0, chunk 0) takes `acc`
+        auto mma_ts_half = [&](uint32_t col, uint32_t acol, uint32_t b, uint32_t acc, int hf) {
             const uint32_t blo = sdesc_lo(b, C::SLAB);
 #pragma unroll
-            for (int kk = 0; kk < TR / 16; ++kk) {
-                const uint32_t a = tmem + acol + ((kk < 4) ? 8u * kk : 64u + 8u * (kk - 4));
-                umma_ts_lo_elect(tmem + col, a, blo + ((kk * 16 * 128) >> 4), IDESC_A, kk > 0 ? 1u : acc);
-            }
+            for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int kk = 4 * gi + 2 * hf + i;
+                    const uint32_t a = tmem + acol + 64u * gi + 8u * (2 * hf + i);
+                    const uint32_t first = (hf == 0 && gi == 0 && i == 0) ? acc : 1u;
+                    umma_ts_lo_elect(tmem + col, a, blo + ((kk * 16 * 128) >> 4), IDESC_A, first);
+                }
         };
         uint32_t fix_cnt = 0, stg = 0, step = 0, acc_cnt = 0;
         bool ok = true;
@@ -753,21 +784,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint32_t t1 = f0 + 2 * j, t2 = t1 + 1, n1 = t1 + 2, n2 = t1 + 3;
                 const bool more = j + 1 < J;
                 if (!DQ) {
-                    ok = wwait(&sm.p_full, step & 1u);
+                    ok = wwait(&sm.p_half[0], step & 1u);
                     if (ok && j == 0) ok = wwait(&sm.acc_empty, (acc_cnt & 1u) ^ 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    mma_ts(C::ACC1, 0, tile_of(t2), j > 0 ? 1u : 0u);  // dV += P^T dO
-                    release(t2);                                        // dO_j: read by dP_j and dV_j
+                    mma_ts_half(C::ACC1, 0, tile_of(t2), j > 0 ? 1u : 0u, 0);  // dV += P^T dO
+                    if (!(ok = wwait(&sm.p_half[1], step & 1u))) break;
+                    tc_fence_after();
+                    mma_ts_half(C::ACC1, 0, tile_of(t2), 1u, 1);
+                    release(t2);  // dO_j: read by dP_j and dV_j
                     if (more) {
                         if (!(ok = wfill(n1))) break;
                         tc_fence_after();
                         mma_ss(0, aF1, tile_of(n1));
                         umma_commit_elect(&sm.s_full);
                     }
-                    if (!(ok = wwait(&sm.ds_full, step & 1u))) break;
+                    if (!(ok = wwait(&sm.ds_half[0], step & 1u))) break;
                     tc_fence_after();
-                    mma_ts(C::ACC2, 128, tile_of(t1), j > 0 ? 1u : 0u);  // dK += dS^T Q
+                    mma_ts_half(C::ACC2, 128, tile_of(t1), j > 0 ? 1u : 0u, 0);  // dK += dS^T Q
+                    if (!(ok = wwait(&sm.ds_half[1], step & 1u))) break;
+                    tc_fence_after();
+                    mma_ts_half(C::ACC2, 128, tile_of(t1), 1u, 1);
                     release(t1);  // Q_j and its extras: read by S_j, dK_j and the element-wise warps
                     if (more) {
                         if (!(ok = wfill(n2))) break;
@@ -784,11 +821,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mma_ss(0, aF1, tile_of(n1));
                         umma_commit_elect(&sm.s_full);
                     }
-                    ok = wwait(&sm.ds_full, step & 1u);
+                    ok = wwait(&sm.ds_half[0], step & 1u);
                     if (ok && j == 0) ok = wwait(&sm.acc_empty, (acc_cnt & 1u) ^ 1u);
                     if (!ok) break;
                     tc_fence_after();
-                    mma_ts(C::ACC1, 128, tile_of(t1), j > 0 ? 1u : 0u);  // dQ += dS K
+                    mma_ts_half(C::ACC1, 128, tile_of(t1), j > 0 ? 1u : 0u, 0);  // dQ += dS K
+                    if (!(ok = wwait(&sm.ds_half[1], step & 1u))) break;
+                    tc_fence_after();
+                    mma_ts_half(C::ACC1, 128, tile_of(t1), 1u, 1);
                     release(t1);                                          // K_j: read by S_j and dQ_j
                     if (more) {
                         if (!(ok = wfill(n2))) break;
