@@ -180,8 +180,8 @@ NCU_TRAFFIC = {
     ("decode", "bf16_decode_b64_h32_sk8192_d128", "2e9e7234d6afbf6e"): 2157160000,
     ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "2e9e7234d6afbf6e"): 1747050000,
     # backward: one-pass captures of the two main launches, printed to five significant figures
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "522315472416dccf"): 339140000,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "522315472416dccf"): 217360000,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "165735717bfcac1f"): 339620000,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "165735717bfcac1f"): 216060000,
 }
 
 
