@@ -40,8 +40,8 @@
 //
 // Causal and window tile skipping ("gfx942 unified attention", section 4): a
 // slot visits only the key tiles that intersect the union of its rows'
-// admissible ranges, last tile first; element masks are applied only on tiles
-// that cut a row's range.  Lazy rescaling: O and l are rescaled only when the running max grows
+// admissible ranges, the last tile first with ALiBi and the first tile first
+// otherwise; element masks are applied only on tiles that cut a row's range.  Lazy rescaling: O and l are rescaled only when the running max grows
 // by more than 8 (base-2 units); otherwise the stale max stays the reference,
 // which keeps every p <= 2^8 and leaves o / l exact.
 #include <cuda_bf16.h>
@@ -63,8 +63,8 @@ constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // base-2 units
 constexpr int LAUNCH_REGS = 128;          // 65536 / 512
 // K/V tiles move through the shared-memory slots in the order the MMA thread
-// reads them, last key tile first: per item K_hi, then (V_u, K_{u-1}) for each
-// tile u > lo, V_lo last.
+// reads them: per item K_first, then (V_u, K_next) for each tile u but the
+// last, V_last last (first_tile / last_tile below give the order).
 // Each of these groups is one MMA step and has one full barrier (the TMA
 // transaction count of its one or two tiles) and one empty barrier (one
 // commit after the step's MMAs), so a step costs the MMA thread one wait and
@@ -243,6 +243,16 @@ __device__ __forceinline__ int item_of(int k, int cta, int grid) {
 }
 
 __device__ __forceinline__ bool slot_live(const Slot& s) { return s.t >= 0 && s.lo <= s.hi; }
+
+// Order of a slot's key tiles: from the last one down (DOWN) or from the
+// first one up.  The recurrence's order is free.  With ALiBi the largest
+// scores sit at the diagonal, so visiting it first settles the running max at
+// once (no rescales); otherwise an item starts on an unmasked tile, whose
+// softmax is the short one, and the masked diagonal tile comes last.
+template <bool DOWN>
+__device__ __forceinline__ int first_tile(const Slot& s) { return DOWN ? s.hi : s.lo; }
+template <bool DOWN>
+__device__ __forceinline__ int last_tile(const Slot& s) { return DOWN ? s.lo : s.hi; }
 __device__ __forceinline__ bool in_range(const Slot& s, int u) { return s.t >= 0 && u >= s.lo && u <= s.hi; }
 
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -310,7 +320,9 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
         float slope_l2 = 0.f;
         if (ALIBI) slope_l2 = __ldg(p.slopes + sl.h) * LOG2E;
         float m_used = -INFINITY, l = 0.f;
-        for (int u = sl.hi; u >= sl.lo; --u) {
+        constexpr bool DOWN = ALIBI;
+        for (int u = first_tile<DOWN>(sl);; u += DOWN ? -1 : 1) {
+            if (DOWN ? u < sl.lo : u > sl.hi) break;
             const bool ok = mbar_wait(&sm.s_full[x], s_cnt & 1, wc, ST_PREFILL_SOFTMAX);
             ++s_cnt;
             if (!__all_sync(0xffffffffu, ok)) return;
@@ -643,13 +655,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ulo = min(ulo, s[x].lo);
                             uhi = max(uhi, s[x].hi);
                         }
-                    // Key tiles are visited from the last one back (the order of the
-                    // recurrence is free; with ALiBi or causal masks the largest scores
-                    // sit near the diagonal, so the running max settles at once).
-                    // groups: (K_hi), then (V_u, K_{u-1}) for u > lo, then (V_lo)
+                    // Key tiles in the order first_tile / last_tile give (down from
+                    // uhi with ALiBi, else up from ulo); groups: (K_first), then
+                    // (V_u, K_next) for every tile u but the last, then (V_last)
+                    constexpr bool DOWN = ALIBI;
                     const int nt = uhi - ulo + 1;
                     for (int i = -1; i < nt && ok; ++i) {
-                        const int u = uhi - i;  // V tile of this group; its K tile is u - 1
+                        const int u = DOWN ? uhi - i : ulo + i;  // V tile of this group
+                        const int un = DOWN ? u - 1 : u + 1;     // its K tile
                         const bool has_v = i >= 0, has_k = i < nt - 1;
                         const int nl = (has_v ? 1 : 0) + (has_k ? 1 : 0);
                         // both slots must have been released by the groups that last used them
@@ -670,7 +683,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const bool is_v = has_v && i == 0;
                             const int st = (ld_cnt + i) % C::NS;
                             uint8_t* dst = sKV + st * C::KV_BYTES;
-                            const int key = (is_v ? u : u - 1) * BN;
+                            const int key = (is_v ? u : un) * BN;
 #pragma unroll
                             for (int hf = 0; hf < C::HALVES; ++hf) {
                                 if (VARLEN)  // packed [total_k][Hkv][D]
@@ -708,6 +721,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
                 return __all_sync(0xffffffffu, mbar_wait(bar, parity, wc, ST_PREFILL_MMA));
             };
+            constexpr bool DOWN = ALIBI;  // key-tile order, as in the producer and softmax roles
             constexpr uint32_t IDESC_S = F16 ? idesc_f16_f32(BM, BN, 0) : idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t IDESC_O = F16 ? idesc_f16_f32(BM, D, 1) : idesc_bf16_f32(BM, D, 1);
             uint32_t ld_cnt = 0, grp_cnt = 0, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0}, o_cnt[2] = {0, 0};
@@ -750,11 +764,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             umma_ss_lo_elect(dS, qlo + off, klo + koff, IDESC_S, kk > 0);
                         }
                         umma_commit_elect(&sm.s_full[x]);
-                        if (ut == s[x].lo) umma_commit_elect(&sm.q_empty[x]);
+                        if (ut == last_tile<DOWN>(s[x])) umma_commit_elect(&sm.q_empty[x]);
                         return true;
                     };
                     if (ulo <= uhi) {
-                        // prologue step: group (K_hi)
+                        const int nt = uhi - ulo + 1;
+                        const int ufirst = DOWN ? uhi : ulo;
+                        // prologue step: group (K_first)
                         uint32_t gb = grp_cnt % NG;
                         ok = wwait(&sm.grp_full[gb], (grp_cnt / NG) & 1);
                         ++grp_cnt;
@@ -762,12 +778,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ld_cnt += 1;
 #pragma unroll
                         for (int x = 0; x < 2 && ok; ++x)
-                            if (in_range(s[x], uhi)) ok = issue_s(x, kst, uhi);
+                            if (in_range(s[x], ufirst)) ok = issue_s(x, kst, ufirst);
                         if (ok) umma_commit_elect(&sm.grp_empty[gb]);
-                        for (int u = uhi; u >= ulo && ok; --u) {
-                            // step u: group (V_u, K_{u-1}); each slot's P V and next
+                        for (int i = 0; i < nt && ok; ++i) {
+                            // step u: group (V_u, K_next); each slot's P V and next
                             // Q K^T then go to the tensor pipe as one run
-                            const bool has_next = u > ulo;
+                            const int u = DOWN ? uhi - i : ulo + i;
+                            const int un = DOWN ? u - 1 : u + 1;
+                            const bool has_next = i < nt - 1;
                             gb = grp_cnt % NG;
                             ok = wwait(&sm.grp_full[gb], (grp_cnt / NG) & 1);
                             ++grp_cnt;
@@ -780,7 +798,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 if (in_range(s[x], u)) {
                                     ok = wwait(&sm.p_full[x], p_cnt[x] & 1);
                                     ++p_cnt[x];
-                                    if (ok && u == s[x].hi) {
+                                    if (ok && u == first_tile<DOWN>(s[x])) {
                                         ok = wwait(&sm.o_empty[x], (o_cnt[x] & 1) ^ 1);
                                         ++o_cnt[x];
                                     }
@@ -788,14 +806,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                     tc_fence_after();
                                     const uint32_t vlo = sdesc_lo(sKVa + vst * C::KV_BYTES, C::KV_SLAB);
                                     const uint32_t dO = tmem + C::O_COL + D * x, aP = tmem + 128u * x;
-                                    const uint32_t acc0 = (u < s[x].hi) ? 1u : 0u;
+                                    const uint32_t acc0 = (u != first_tile<DOWN>(s[x])) ? 1u : 0u;
 #pragma unroll
                                     for (int kk = 0; kk < BN / 16; ++kk)
                                         umma_ts_lo_elect(dO, aP + 8u * kk, vlo + ((kk * 16 * 128) >> 4), IDESC_O,
                                                          kk > 0 ? 1u : acc0);
-                                    if (u == s[x].lo) umma_commit_elect(&sm.o_full[x]);
+                                    if (u == last_tile<DOWN>(s[x])) umma_commit_elect(&sm.o_full[x]);
                                 }
-                                if (has_next && in_range(s[x], u - 1)) ok = issue_s(x, kst, u - 1);
+                                if (has_next && in_range(s[x], un)) ok = issue_s(x, kst, un);
                             }
                             if (!ok) break;
                             umma_commit_elect(&sm.grp_empty[gb]);
