@@ -173,13 +173,13 @@ KERNEL_SOURCES = {
     "backward": ("backward_bf16.cu", "ptx.cuh", "kernels.h"),
 }
 NCU_TRAFFIC = {
-    # (kernel, workload, source fingerprint): bytes per launch
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "96829f447537020b"): 128985600,
-    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "96829f447537020b"): 4025290000,
-    # decode: full-size one-pass captures, printed to three or four significant figures
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "2e9e7234d6afbf6e"): 2157160000,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "2e9e7234d6afbf6e"): 1747050000,
-    # backward: one-pass captures of the two main launches, printed to five significant figures
+    # (kernel, workload, source fingerprint): bytes per launch, one-pass ncu
+    # captures of the full-size workloads (values as ncu prints them: three to
+    # five significant figures)
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "a54dfc84dcb7c58b"): 129950000,
+    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "a54dfc84dcb7c58b"): 4105060000,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "d2740f33f2be2b02"): 2156490000,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "d2740f33f2be2b02"): 1746920000,
     ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "165735717bfcac1f"): 339620000,
     ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "165735717bfcac1f"): 216060000,
 }
