@@ -335,6 +335,16 @@ def bench_decode(g, args, ws, dev, pk):
                         "traffic": None if args.decode_b else ncu_traffic("decode", w.name),
                         "peak_source": f"hbm_gbs ({pk['source']})", "frac_of_8tbs_nominal": round(gbs / 8000.0, 4)}}
     res["graph"] = decode_graph_timing(fn, args, ws, stream)
+    if ws == 1 and not args.no_cpu_baseline:
+        # the float64 oracle on batch 0 of the same inputs (its Q + K + V + O bytes per second)
+        import oracle
+        qb, kb, vb = x["q"][:1].cpu(), x["k"][:1].cpu(), x["v"][:1].cpu()
+        t0 = time.time()
+        oracle.decode(qb, kb, vb, scale=w.scale)
+        dt = time.time() - t0
+        nb = 2 * qb.numel() * 2 + kb.numel() * 2 + vb.numel() * 2
+        res["cpu_baseline"] = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.max_threads(),
+                               "kind": "oracle", "sample": f"batch 0 of {w.B}: {w.Hq} query rows ({dt:.2f} s)"}
     if not args.no_e2e:
         qh = x["q"].cpu().pin_memory()
         kh = x["k"].cpu().pin_memory()
@@ -441,7 +451,22 @@ def bench_varlen(g, args, ws, dev, pk):
     per = ms / args.steps
     flops = 4.0 * c["D"] * c["Hq"] * sum(n * (n + 1) / 2 for n in lens)
     tf = flops / (per * 1e-3) / 1e12
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        # the float64 oracle on the shortest packed sequence of the same inputs
+        import oracle
+        b = min(range(len(lens)), key=lambda i: lens[i])
+        a0, a1 = int(cu[b]), int(cu[b + 1])
+        cs = torch.tensor([0, a1 - a0], dtype=torch.int32)
+        t0 = time.time()
+        oracle.attn_varlen(q[a0:a1].cpu(), k[a0:a1].cpu(), v[a0:a1].cpu(), cs, cs, causal=True)
+        dt = time.time() - t0
+        n = a1 - a0
+        cpu = {"value": round(4.0 * c["D"] * c["Hq"] * n * (n + 1) / 2 / dt / 1e12, 6), "unit": "TFLOP/s",
+               "cores": torch.get_num_threads(), "kind": "oracle",
+               "sample": f"sequence {b} ({n} tokens, all {c['Hq']} heads; {dt:.1f} s)"}
     return {"workload": varlen_workload_name(), "metric": "varlen causal prefill TFLOP/s (causal-adj)",
+            "cpu_baseline": cpu,
             "value": round(tf * ws, 2), "unit": "TFLOP/s", "ms_per_step": round(per, 4), "flops_per_step": flops,
             "total_tokens": T, "gpu_launches": args.steps,
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
@@ -497,6 +522,17 @@ def bench_backward(g, args, ws, dev, pk):
     *_, phases = g.attn_bwd(q, k, v, do, out, lse, causal=True, dq=dq, dk=dk, dv=dv, workspace=wsb,
                             phase_times_reps=args.steps)
     _, prep_ms, dkdv_ms, dq_ms = phases
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        # the float64 backward oracle on one (batch, kv group) slice of the same inputs
+        import oracle
+        G = Hq // Hkv
+        t0 = time.time()
+        oracle.attn_bwd(q[:1, :G].cpu(), k[:1, :1].cpu(), v[:1, :1].cpu(), do[:1, :G].cpu(), causal=True)
+        dt = time.time() - t0
+        cpu = {"value": round(10.0 * D * G * S * (S + 1) / 2 / dt / 1e12, 6), "unit": "TFLOP/s",
+               "cores": torch.get_num_threads(), "kind": "oracle",
+               "sample": f"batch 0, kv head 0 and its {G} query heads ({dt:.1f} s)"}
     tf_a = 8.0 * D * pairs / (dkdv_ms * 1e-3) / 1e12  # S, dP, dV, dK
     tf_b = 6.0 * D * pairs / (dq_ms * 1e-3) / 1e12    # S, dP, dQ
     name = bwd_workload_name()
@@ -505,6 +541,7 @@ def bench_backward(g, args, ws, dev, pk):
             "flops_convention": "5 products x 2 D per admissible pair; the pages' cost line counts 12 D "
                                 "(a 4 D forward recompute)",
             "gpu_launches": 4 * args.steps,
+            "cpu_baseline": cpu,
             "phase_ms": {"prep": round(prep_ms, 4), "dkdv": round(dkdv_ms, 4), "dq": round(dq_ms, 4)},
             "roofline": {"bound": "tensor", "kernel": "bwd_kernel dK/dV (S, dP, dV, dK: 8 D flops per pair)",
                          "achieved": round(tf_a, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
