@@ -10,7 +10,7 @@
 // where Delta_i = sum_j P_ij dP_ij = dO_i . O_i (O the forward output), and
 // dK / dV of a kv head sum over the query heads of its GQA group.
 //
-// Three launches, all deterministic (no atomics, fixed summation order):
+// Four launches, all deterministic (no atomics, fixed summation order):
 //   bwd_rows_kernel    per query row its admissible key interval [a, e]
 //                      (causal, window, row bounds, Sk) and per 128-row query
 //                      tile a summary: the span of its live rows' intervals
@@ -50,11 +50,15 @@
 //   [dS_j] dK += dS_j Q_j, dP_{j+1}
 // DQ = 1:
 //   S_0, dP_0, then per step j: [S_j read] S_{j+1}, [dS_j] dQ += dS_j K_j, dP_{j+1}
-// P and dS are handed over in two halves of each group's columns, each with
-// its own barrier; the MMAs reading a half go out as soon as it is in TMEM.
-// ([x] = wait for the element-wise warps).  tcgen05 operations issued by one
+// ([x] = wait for the element-wise warps).  P and dS are handed over in two
+// halves of each group's columns, each with its own barrier; the MMAs reading
+// a half go out as soon as it is in TMEM.  tcgen05 operations issued by one
 // thread execute in order, so an MMA that overwrites a TMEM tile is issued
 // after the MMA that reads the tile's previous contents.
+//
+// Item boundaries: the producer fetches an item's first streamed tiles before
+// its fixed tiles (which wait until the previous item's MMAs are done with
+// theirs) and prefetches the next item's fixed tiles into L2.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
