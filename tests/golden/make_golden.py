@@ -35,6 +35,18 @@ CASES = [
          cite="attention.fkc.md, attention_naive: softcap tanh(s/c)*c, then ALiBi slope*(kj-qi); window; fully-masked row -> zeros"),
 ]
 
+# Backward by recompute (attention.fkc.md, attention_flash_backward): dQ, dK, dV
+# for a seeded dO, expected values from oracle.attn_bwd alone.
+BWD_CASES = [
+    dict(name="bwd_gqa_causal_bf16", B=1, Hq=4, Hkv=2, Sq=7, Sk=7, D=8, dtype="bf16",
+         causal=True, wl=None, wr=None, softcap=None, alibi=False, empty=0.0,
+         cite="attention.fkc.md, attention_flash_backward: recompute P, dV, dP, dS, dQ, dK; GQA sums"),
+    dict(name="bwd_window_softcap_alibi_f32", B=1, Hq=2, Hkv=1, Sq=8, Sk=9, D=4, dtype="f32",
+         causal=True, wl=3, wr=None, softcap=2.0, alibi=True, empty=0.25,
+         cite="attention.fkc.md, attention_flash_backward: softcap factor 1 - tanh^2(s_pre/c); "
+              "a fully-masked row contributes nothing"),
+]
+
 DT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 
@@ -56,7 +68,21 @@ def run(c):
                        softcap=c["softcap"], alibi_slopes=slopes, row_kv_bounds=rb, return_lse=True)
 
 
+def run_bwd(c):
+    q, k, v, slopes, rb = inputs(c)
+    do = synth.normal((c["B"], c["Hq"], c["Sq"], c["D"]), 7, synth.STREAM_DO, DT[c["dtype"]])
+    return oracle.attn_bwd(q, k, v, do, causal=c["causal"], window_left=c["wl"], window_right=c["wr"],
+                           softcap=c["softcap"], alibi_slopes=slopes, row_kv_bounds=rb)
+
+
 def main():
+    for c in BWD_CASES:
+        rec = dict(c)
+        for name, t in zip(("dq", "dk", "dv"), run_bwd(c)):
+            rec[name] = [float.hex(x) for x in t.reshape(-1).tolist()]
+        with open(os.path.join(HERE, c["name"] + ".json"), "w") as f:
+            json.dump(rec, f, indent=0)
+            f.write("\n")
     for c in CASES:
         out, lse = run(c)
         rec = dict(c)

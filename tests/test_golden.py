@@ -34,3 +34,16 @@ def test_golden_fixture(case):
             assert g == w
         else:
             assert abs(g - w) <= 1e-13
+
+
+@pytest.mark.parametrize("case", make_golden.BWD_CASES, ids=lambda c: c["name"])
+def test_golden_backward_fixture(case):
+    with open(os.path.join(HERE, case["name"] + ".json")) as f:
+        rec = json.load(f)
+    assert rec["cite"]
+    for name, t in zip(("dq", "dk", "dv"), make_golden.run_bwd(case)):
+        want = [float.fromhex(x) for x in rec[name]]
+        got = t.reshape(-1).tolist()
+        assert len(got) == len(want) and any(w != 0.0 for w in want)
+        for g, w in zip(got, want):
+            assert abs(g - w) <= 1e-12
