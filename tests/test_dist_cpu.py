@@ -58,3 +58,22 @@ def test_reference_arm_prints_once_under_torchrun():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
     assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_traffic_fingerprint_ignores_comments_only():
+    # roofline.traffic is reported only while the kernel sources match the
+    # capture: comment or whitespace edits keep the fingerprint, code edits do not
+    sys.path.insert(0, ROOT)
+    import bench
+    src = {f: open(os.path.join(ROOT, "tiled_scaled_dot_gb300", "csrc", f)).read()
+           for f in bench.KERNEL_SOURCES["backward"]}
+    base = bench.kernel_fingerprint("backward", read=lambda f: src[f])
+    assert base == bench.kernel_fingerprint("backward")
+    f0 = bench.KERNEL_SOURCES["backward"][0]
+    commented = dict(src)
+    commented[f0] = "// a new comment\n/* and a block\n comment */\n" + src[f0].replace("\n", "\n\n", 3)
+    assert bench.kernel_fingerprint("backward", read=lambda f: commented[f]) == base
+    changed = dict(src)
+    changed[f0] = src[f0].replace("constexpr int TR = 128;", "constexpr int TR = 64;")
+    assert changed[f0] != src[f0]
+    assert bench.kernel_fingerprint("backward", read=lambda f: changed[f]) != base
