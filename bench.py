@@ -13,7 +13,12 @@ A step is one pass of the hot path over one batch of synthetic input:
   * varlen prefill (reported beside it): attn_fwd_varlen on 32 packed causal
     sequences of seeded lengths 512..4096;
   * backward (reported beside it): attn_bwd on the headline shape with the
-    forward's out and lse given (dQ, dK, dV; 10 D flops per admissible pair).
+    forward's out and lse given (dQ, dK, dV; 10 D flops per admissible pair);
+  * long causal prefill (reported beside it): attn_fwd on bf16 causal B=1,
+    Hq=32, Hkv=8, S=8192, D=128, timed like the headline;
+  * masked prefill (reported beside it): attn_fwd on bf16 B=2, Hq=Hkv=16,
+    S=4096, D=64, causal with window (1024, 0), softcap 50, ALiBi and 82
+    empty rows, timed like the headline.
 value = causal-adjusted attention TFLOP/s (4 D flops per admissible
 (query, key) pair) over all ranks.  The decode object reports HBM GB/s of its
 algorithmic bytes (Q + K + V + O).
@@ -47,6 +52,8 @@ from synth.workloads import WORKLOADS, make_inputs  # noqa: E402
 METRIC = "attn fwd TFLOP/s (causal-adj) & decode HBM GB/s, % of roofline, 1×GB300"
 PREFILL = "bf16_causal_b4_h32_s2048_d128"
 DECODE = "bf16_decode_b64_h32_sk8192_d128"
+LONG = "bf16_causal_b1_h32_s8192_d128"
+MASKED = "bf16_masked_b2_h16_s4096_d64"
 L2_BYTES = 126 * 1024 * 1024
 
 
@@ -64,6 +71,8 @@ def parse():
     ap.add_argument("--no-paged", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-backward", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the S=8192 causal prefill object")
+    ap.add_argument("--no-masked", action="store_true", help="skip the masked D=64 prefill object")
     ap.add_argument("--profile", choices=["prefill", "decode", "both", "paged", "varlen", "backward"], default=None,
                     help="launch warm-up + steps of one path and exit (for ncu); no timing, one input copy")
     ap.add_argument("--decode-b", type=int, default=None, help="override the decode batch (smaller ncu captures)")
@@ -170,9 +179,10 @@ def max_over_ranks(x: float, ws: int) -> float:
 # reports null until it is captured again.  The captures and their commands
 # are summarised under profiles/.
 KERNEL_SOURCES = {
-    "prefill": ("prefill_bf16.cu", "ptx.cuh", "kernels.h"),
-    "decode": ("decode_bf16.cu", "ptx.cuh", "kernels.h"),
-    "backward": ("backward_bf16.cu", "ptx.cuh", "kernels.h"),
+    # api.cu chooses the tensor-map boxes, grids and split plans of every launch
+    "prefill": ("prefill_bf16.cu", "ptx.cuh", "kernels.h", "api.cu"),
+    "decode": ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu"),
+    "backward": ("backward_bf16.cu", "ptx.cuh", "kernels.h", "api.cu"),
 }
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch, one-pass ncu
@@ -188,12 +198,14 @@ NCU_TRAFFIC = {
 
 
 def source_tokens(text):
-    """C/C++ source without comments and whitespace: what the compiler sees
-    of it, so that an edit to a comment keeps a kernel's fingerprint."""
+    """C/C++ source without comments, each run of whitespace collapsed to one
+    space: what the compiler sees of it, so that an edit to a comment or to
+    indentation keeps a kernel's fingerprint while `a - -b` and `a--b` stay
+    different programs."""
     import re
     text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     text = re.sub(r"//[^\n]*", " ", text)
-    return "".join(text.split())
+    return " ".join(text.split())
 
 
 def kernel_fingerprint(kind, read=None):
@@ -246,7 +258,7 @@ def soak(fn, seconds):
     torch.cuda.synchronize()
 
 
-def bench_prefill(g, w, args, ws, dev, pk):
+def bench_prefill(g, w, args, ws, dev, pk, e2e=True):
     stream = torch.cuda.current_stream()
     base = make_inputs(w, dev)
     in_bytes = sum(t.numel() * t.element_size() for k, t in base.items() if k in ("q", "k", "v"))
@@ -275,10 +287,31 @@ def bench_prefill(g, w, args, ws, dev, pk):
     res["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": pk["bf16"], "unit": "TFLOP/s",
                        "frac": round(tflops / pk["bf16"], 4), "traffic": ncu_traffic("prefill", w.name),
                        "peak_source": f"bf16_tflops ({pk['source']}, burst: the kernel is timed alone)"}
-    if not args.no_e2e:
+    if e2e and not args.no_e2e:
         res["e2e"] = e2e_prefill(g, w, base, args, ws, stream, flops)
     del sets, outs
     return res
+
+
+def bench_prefill_object(g, name, args, ws, dev, pk, what, bound_note=None):
+    """Another forward workload, timed exactly like the headline (inputs
+    rotated past L2, a soak, CUDA events on the launching stream), with its
+    own roofline and a bounded oracle sample as its CPU baseline."""
+    w = WORKLOADS[name]
+    r = bench_prefill(g, w, args, ws, dev, pk, e2e=False)
+    obj = {"workload": name, "metric": what, "value": round(r["tflops_per_gpu"] * ws, 2), "unit": "TFLOP/s",
+           "ms_per_step": round(r["ms_per_step"], 4), "flops_per_step": r["flops"],
+           "dense_flops_per_step": r["dense_flops"], "gpu_launches": args.steps,
+           "l2": f"inputs rotated over {r['rotation']} copies ({r['in_bytes'] / 2**20:.0f} MiB each)",
+           "roofline": r["roofline"]}
+    if bound_note:
+        obj["roofline"]["limiter"] = bound_note
+    if ws == 1 and not args.no_cpu_baseline:
+        x_cpu = make_inputs(w, "cpu")
+        tf, sample, threads = oracle_sample(w, x_cpu, min(args.cpu_seconds, 5.0))
+        obj["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                               "sample": sample}
+    return obj
 
 
 def e2e_prefill(g, w, base, args, ws, stream, flops):
@@ -367,6 +400,11 @@ def bench_decode(g, args, ws, dev, pk):
                       "h2d_bytes_per_step": qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2,
                       "d2h_bytes_per_step": oh.numel() * 2, "ms_per_step": round(per2, 4)}
     return res
+
+
+# What bounds the masked D=64 workload below the tensor roofline (the
+# counters behind it are summarised under profiles/).
+MASKED_LIMITER = None
 
 
 PAGED_SHAPE = dict(B=64, Hq=32, Hkv=8, D=128, block_size=64, ctx_lo=4096, ctx_hi=8192)
@@ -681,6 +719,11 @@ def main():
         paged = None if args.no_paged else bench_decode_paged(g, args, ws, dev, pk)
         varl = None if args.no_varlen else bench_varlen(g, args, ws, dev, pk)
         bwd = None if args.no_backward else bench_backward(g, args, ws, dev, pk)
+        long_ = None if args.no_long or w.name == LONG else bench_prefill_object(
+            g, LONG, args, ws, dev, pk, "long causal prefill TFLOP/s (causal-adj)")
+        masked = None if args.no_masked or w.name == MASKED else bench_prefill_object(
+            g, MASKED, args, ws, dev, pk, "masked prefill TFLOP/s (admissible pairs: causal, window, row bounds)",
+            MASKED_LIMITER)
     finally:
         clocks = sampler.stop()
     if g.device_status() != 0:
@@ -710,6 +753,10 @@ def main():
         line["varlen"] = varl
     if bwd is not None:
         line["backward"] = bwd
+    if long_ is not None:
+        line["long_causal"] = long_
+    if masked is not None:
+        line["masked"] = masked
     if rank == 0 and not args.no_cpu_baseline:
         x_cpu = make_inputs(w, "cpu")
         tf, sample, threads = oracle_sample(w, x_cpu, args.cpu_seconds)

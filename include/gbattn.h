@@ -34,6 +34,10 @@
  * memory in any call; it keeps a small host cache of TMA descriptors.  Calls
  * enqueue work on `stream` (a cudaStream_t; NULL = the legacy default stream)
  * and return without synchronising.  `out` must not overlap any input.
+ * The library looks up the device addresses of its own module variables (the
+ * status word, the scratch array of attn_decode_noalloc) once per device and
+ * keeps them: a cudaDeviceReset may move them, so a process must not call the
+ * library on a device after resetting it.
  *
  * Errors: every call returns a status code and never aborts the process.
  * Argument errors are detected on the host before anything is launched.
@@ -192,8 +196,11 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
  * attn_decode, minus workspace / workspace_bytes.
  *
  * The split partials go to a fixed scratch array of GBATTN_NOALLOC_SCRATCH_BYTES
- * that the library keeps in device memory on every GPU that loads it, until
- * the process exits.  Nothing is allocated by this call.  A problem whose
+ * in the library's own device module.  Under CUDA's default lazy module
+ * loading the array occupies device memory on each GPU where this entry has
+ * been called (its module loads on first use); with eager loading
+ * (CUDA_MODULE_LOADING=EAGER) on each GPU where the library is loaded.  It is
+ * held until the process exits.  Nothing is allocated by this call.  A problem whose
  * workspace (attn_decode_workspace_size) exceeds that size returns
  * GBATTN_ERR_UNSUPPORTED; use attn_decode with your own workspace then.
  * All calls share the one array and it keeps the last call's contents, so

@@ -77,3 +77,8 @@ def test_traffic_fingerprint_ignores_comments_only():
     changed[f0] = src[f0].replace("constexpr int TR = 128;", "constexpr int TR = 64;")
     assert changed[f0] != src[f0]
     assert bench.kernel_fingerprint("backward", read=lambda f: changed[f]) != base
+    # whitespace between tokens can be meaningful: `a - -b` is not `a--b`
+    assert bench.source_tokens("x = a - -b;") != bench.source_tokens("x = a--b;")
+    assert bench.source_tokens("x  =\n\ta - -b;  // c") == bench.source_tokens("x = a - -b;")
+    # the launch parameters chosen in api.cu are part of every kernel's fingerprint
+    assert all("api.cu" in srcs for srcs in bench.KERNEL_SOURCES.values())

@@ -8,8 +8,12 @@
 // a fixed array in device memory that is part of the library's own module, so
 // the caller passes only inputs and outputs and nothing is allocated per call.
 //
-// The array is GBATTN_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU that loads the
-// library, held until the process exits.  Every call shares it: a call that
+// The array is GBATTN_NOALLOC_SCRATCH_BYTES (32 MiB).  It occupies device
+// memory on each GPU where this file's module has been loaded -- under CUDA's
+// default lazy loading, where attn_decode_noalloc has been called -- until the
+// process exits.  Its device address is looked up once per device and kept, so
+// the entry must not be used on a device after a cudaDeviceReset (the module
+// may be reloaded elsewhere).  Every call shares the array: a call that
 // overlaps another on the GPU (two streams, or two host threads) races on it.
 // Nothing in it needs to start at zero: each call writes every partial result
 // its combine step reads before reading it.

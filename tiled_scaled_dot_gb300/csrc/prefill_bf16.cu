@@ -269,7 +269,13 @@ __device__ __forceinline__ float tanh_approx(float x) {
 
 struct Smem {
     uint64_t q_full[2], q_empty[2];
-    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2], l_full[2];
+    uint64_t s_full[2], p_full[2], o_full[2], o_empty[2];
+    // l_full[e][x]: entry e of slot x's (l, m) hand-off is written.  One barrier
+    // per entry: a slot whose next item has a single key tile finishes that
+    // item's softmax without waiting for any P V, so it can publish item n + 1
+    // before the epilogue has waited for item n; with one barrier per slot the
+    // barrier would then be two phases ahead of the epilogue's parity wait.
+    uint64_t l_full[2][2];
     uint64_t grp_full[NG], grp_empty[NG];  // one per step group of K/V tiles
     uint64_t item_full[NI], item_empty[NI];
     uint64_t drain;
@@ -425,7 +431,7 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
         sm.l_buf[par][x][r] = l;
         sm.m_buf[par][x][r] = m_used;
         ++l_cnt;
-        mbar_arrive(&sm.l_full[x]);
+        mbar_arrive(&sm.l_full[par][x]);
     }
 }
 
@@ -472,9 +478,9 @@ __device__ __forceinline__ void epilogue_role(const Params& p, Smem& sm, uint32_
                 }
                 continue;
             }
-            bool ok = mbar_wait(&sm.l_full[x], cnt[x] & 1, wc, ST_PREFILL_EPILOGUE);
-            ok = ok && mbar_wait(&sm.o_full[x], cnt[x] & 1, wc, ST_PREFILL_EPILOGUE);
             const int par = cnt[x] & 1;
+            bool ok = mbar_wait(&sm.l_full[par][x], (cnt[x] >> 1) & 1, wc, ST_PREFILL_EPILOGUE);
+            ok = ok && mbar_wait(&sm.o_full[x], cnt[x] & 1, wc, ST_PREFILL_EPILOGUE);
             ++cnt[x];
             if (!__all_sync(0xffffffffu, ok)) return;
             tc_fence_after();
@@ -557,7 +563,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(&sm.p_full[x], BM);
             mbar_init(&sm.o_full[x], 1);
             mbar_init(&sm.o_empty[x], BM);
-            mbar_init(&sm.l_full[x], BM);
+            mbar_init(&sm.l_full[0][x], BM);
+            mbar_init(&sm.l_full[1][x], BM);
         }
         for (int i = 0; i < NG; ++i) {
             mbar_init(&sm.grp_full[i], 1);
