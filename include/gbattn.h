@@ -163,19 +163,30 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* 
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Sk, int D, int num_splits);
 
 /*
- * attn_decode -- decode step: one query row per (b, h) against all Sk keys.
+ * attn_decode -- decode step: one query row per (b, h), the newest token of
+ * its sequence, against the Sk keys before it.
  * "gfx942 unified attention", section 4 (decode runs non-causal: the single
  * query sees every key) and section 8 (split-KV: the keys are split across
  * thread blocks and the partial softmax-weighted outputs combined).  The
  * combine is the online recurrence of section 3 applied across splits, in a
  * fixed split order, so reruns are bitwise identical.
  *
+ * The query sits at position Sk - 1, the last key (the alignment under which a
+ * non-causal single row is the causal one, and the decode position of
+ * attention.fkc.md, attention_paged_naive): the ALiBi term is
+ * alibi_slopes[h] * (j - (Sk - 1)), and the window of the dense contract
+ * (attention.fkc.md, header: window_size_left/right) admits keys
+ * j >= Sk - 1 - window_left; no key lies after the query, so window_right
+ * admits every key.  Tiles before the window are not read.
+ *
  *  q              device [B, Hq, 1, D]; k, v device [B, Hkv, Sk, D].
- *  alibi_slopes   device fp32 [Hq] or NULL; the query position is i = 0.
+ *  alibi_slopes   device fp32 [Hq] or NULL.
  *  out            device [B, Hq, 1, D]; lse_out device fp32 [B, Hq] or NULL.
  *  softcap        0 = none, else > 0.
+ *  window_left, window_right   -1 = unbounded (None), else >= 0.
  *  num_splits     0 = automatic; else the number of key chunks (each chunk is a
- *                 multiple of 64 keys; chunks past the end are empty).
+ *                 multiple of 64 keys; chunks past the end are empty).  With a
+ *                 left window the chunks cover the window's keys only.
  *  workspace      device scratch of at least
  *                 attn_decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits)
  *                 bytes, 16-byte aligned (may be NULL when that size is 0).
@@ -184,8 +195,8 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Sk, int D, int num
  *  D              64 or 128.
  */
 int attn_decode(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, float* lse_out,
-                int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap, int num_splits,
-                void* workspace, size_t workspace_bytes, int dtype, void* stream);
+                int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap, int window_left,
+                int window_right, int num_splits, void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
 /*
  * attn_decode_noalloc -- attn_decode without a caller-provided workspace.
@@ -193,7 +204,7 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
  * that cannot allocate device memory themselves (an engine whose own pool owns
  * all device memory, or a latency-critical loop that must not call cudaMalloc,
  * which can synchronise the device).  Same arguments and results as
- * attn_decode, minus workspace / workspace_bytes.
+ * attn_decode without a window, minus workspace / workspace_bytes.
  *
  * The split partials go to a fixed scratch array of GBATTN_NOALLOC_SCRATCH_BYTES
  * in the library's own device module.  Under CUDA's default lazy module
@@ -222,9 +233,11 @@ int attn_decode_noalloc(const void* q, const void* k, const void* v, const float
  * logical positions k_pos = 0 .. context_lens[b] - 1, key k_pos living in pool
  * block block_table[b, k_pos / block_size], row k_pos % block_size.  The query
  * sits at abs_pos = context_lens[b] - 1, so every key of the context is
- * admissible and the ALiBi term is slope_h * (k_pos - abs_pos).  A sequence
- * with context length 0 outputs the zero row (lse -inf).  Split-KV over keys
- * and the log-sum-exp combine as in attn_decode.
+ * admissible and the ALiBi term is slope_h * (k_pos - abs_pos).  An optional
+ * left window (the dense contract's window_size_left at abs_pos) admits only
+ * keys k_pos >= abs_pos - window_left; window_right admits every key.  A
+ * sequence with context length 0 outputs the zero row (lse -inf).  Split-KV
+ * over keys and the log-sum-exp combine as in attn_decode.
  *
  *  q              device [B, Hq, 1, D] (bf16 or fp16, see dtype).
  *  k_cache, v_cache  device pools [num_blocks, block_size, Hkv, D], same type.
@@ -249,8 +262,8 @@ size_t attn_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_blocks_p
 int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const uint32_t* block_table,
                       const uint32_t* context_lens, const float* alibi_slopes, void* out, float* lse_out, int B,
                       int Hq, int Hkv, int D, int num_blocks, int block_size, int max_blocks_per_seq,
-                      float softmax_scale, float softcap, int num_splits, void* workspace, size_t workspace_bytes,
-                      int dtype, void* stream);
+                      float softmax_scale, float softcap, int window_left, int window_right, int num_splits,
+                      void* workspace, size_t workspace_bytes, int dtype, void* stream);
 
 /*
  * attn_bwd -- attention backward by recompute (attention.fkc.md,

@@ -9,8 +9,9 @@ share no code.
 "attention_naive"); ``attn_tiled`` runs the streaming online-softmax
 recurrence (attention.fkc.md, "attention_flash"; "gfx942 unified attention",
 section 3) in float64 and exists to cross-check the first.  Decode is the same
-definition with one query row and no causal mask ("gfx942 unified attention",
-section 4, last paragraph), so ``decode`` calls ``attn`` with Sq = 1.
+definition with one query row at the last position, Sk - 1 ("gfx942 unified
+attention", section 4: decode runs non-causal, the same as causal at the last
+row), so ``decode`` calls ``attn`` with Sq = 1 and that query position.
 
 ``attn_paged`` is paged-cache attention (attention.fkc.md,
 "attention_paged_naive"): keys and values read through a per-sequence block
@@ -69,7 +70,7 @@ def _load():
             I = ctypes.c_int
             L = ctypes.c_long
             Dd = ctypes.c_double
-            lib.oracle_attn_rows.argtypes = [I, P, P, P, P, P, I, I, I, I, I, I, Dd, I, L, L, Dd,
+            lib.oracle_attn_rows.argtypes = [I, P, P, P, P, P, I, I, I, I, I, I, Dd, I, L, L, Dd, L,
                                              P, ctypes.c_int64, P, P, I]
             lib.oracle_attn_rows.restype = I
             lib.oracle_attn_tiled.argtypes = [I, P, P, P, P, P, I, I, I, I, I, I, Dd, I, L, L, Dd,
@@ -118,13 +119,15 @@ def _win(w):
 
 def attn(q, k, v, *, scale=None, causal=False, window_left=None, window_right=None,
          softcap=None, alibi_slopes=None, row_kv_bounds=None, rows=None, threads=0,
-         return_lse=False):
+         return_lse=False, query_pos0=0):
     """Materialised float64 attention.
 
     q [B,Hq,Sq,D], k/v [B,Hkv,Sk,D] (bf16, f32 or f64, any device: copied to
     the host).  ``rows`` (optional 1-D int64 of flat (b*Hq + h)*Sq + qi
     indices) restricts the work to those rows; the result is then [n, D].
-    Returns float64 out (and lse if asked).
+    Query row qi sits at position ``query_pos0 + qi`` for the causal and
+    window masks and the ALiBi term (0: the top-left alignment of
+    position_admissible).  Returns float64 out (and lse if asked).
     """
     q, k, v, s, rb, (B, Hq, Hkv, Sq, Sk, D) = _prep(q, k, v, alibi_slopes, row_kv_bounds)
     if scale is None:
@@ -143,7 +146,7 @@ def attn(q, k, v, *, scale=None, causal=False, window_left=None, window_right=No
     rc = _load().oracle_attn_rows(_DT[q.dtype], _ptr(q), _ptr(k), _ptr(v), _ptr(s), _ptr(rb),
                                   B, Hq, Hkv, Sq, Sk, D, _f32(scale), int(bool(causal)),
                                   _win(window_left), _win(window_right),
-                                  0.0 if not softcap else _f32(softcap),
+                                  0.0 if not softcap else _f32(softcap), int(query_pos0),
                                   _ptr(rr), n, _ptr(out), _ptr(lse), int(threads))
     if rc:
         raise ValueError("oracle rejected the problem")
@@ -169,17 +172,26 @@ def attn_tiled(q, k, v, *, BR=16, BC=16, scale=None, causal=False, window_left=N
     return (out, lse) if return_lse else out
 
 
-def decode(q, k, v, *, scale=None, softcap=None, alibi_slopes=None, rows=None, threads=0,
-           return_lse=False):
-    """Decode: one query row per (b, h) attending to every key, no causal mask."""
+def decode(q, k, v, *, scale=None, softcap=None, alibi_slopes=None, window_left=None, window_right=None,
+           rows=None, threads=0, return_lse=False):
+    """Decode: one query row per (b, h), the newest token of its sequence.
+
+    The row sits at position Sk - 1, after every key ("gfx942 unified
+    attention", section 4: decode runs non-causal, which at the last position
+    is the causal mask; attention_paged_naive puts the decode query at
+    context_len - 1 the same way).  The ALiBi term is slope_h (j - (Sk - 1));
+    a left window admits keys j >= Sk - 1 - window_left; a right window admits
+    every key (none lies after the query).
+    """
     if q.shape[2] != 1:
         raise ValueError("decode takes Sq == 1")
     return attn(q, k, v, scale=scale, causal=False, softcap=softcap, alibi_slopes=alibi_slopes,
-                rows=rows, threads=threads, return_lse=return_lse)
+                window_left=window_left, window_right=window_right, rows=rows, threads=threads,
+                return_lse=return_lse, query_pos0=k.shape[2] - 1)
 
 
 def attn_paged(q, k_cache, v_cache, block_table, context_lens, *, scale=None, softcap=None,
-               alibi_slopes=None, return_lse=False):
+               alibi_slopes=None, window_left=None, window_right=None, return_lse=False):
     """Paged-cache attention in float64 (attention.fkc.md, "attention_paged_naive").
 
     q [B, Hq, Sq, D]; k_cache, v_cache [num_blocks, block_size, Hkv, D];
@@ -188,7 +200,10 @@ def attn_paged(q, k_cache, v_cache, block_table, context_lens, *, scale=None, so
     key k_pos living at pool block block_table[b, k_pos // block_size], row
     k_pos % block_size, kv head h // (Hq / Hkv).  The query's absolute position
     is abs_pos = max(context_lens[b] - Sq, 0) + q_pos (the saturating
-    subtraction of the contract); keys after it are masked.  Scores: scale q.k,
+    subtraction of the contract); keys after it are masked, and so are keys
+    outside the optional sliding window [abs_pos - window_left, abs_pos +
+    window_right] (the dense contract's window, at the query's absolute
+    position; None or -1: unbounded).  Scores: scale q.k,
     then softcap c tanh(s / c), then + slope_h (k_pos - abs_pos); a stable
     softmax and the weighted sum of V rows.  A row with no admissible key is
     the zero row with lse = -inf.  A physical block index >= num_blocks is an
@@ -226,6 +241,10 @@ def attn_paged(q, k_cache, v_cache, block_table, context_lens, *, scale=None, so
         Kb, Vb = K[blk, off], V[blk, off]  # [ctx, Hkv, D]: the gathered keys in logical order
         abs_pos = max(ctx - Sq, 0) + torch.arange(Sq, dtype=torch.int64)  # [Sq]
         admissible = pos[None, :] <= abs_pos[:, None]  # [Sq, ctx]
+        if window_left is not None and window_left >= 0:
+            admissible &= pos[None, :] >= abs_pos[:, None] - window_left
+        if window_right is not None and window_right >= 0:
+            admissible &= pos[None, :] <= abs_pos[:, None] + window_right
         for h in range(Hq):
             g = h // G
             s = sc * (q[b, h] @ Kb[:, g, :].T)  # [Sq, ctx]

@@ -13,14 +13,20 @@
  *
  *   s_j = scale * sum_d Q[b,h,qi,d] * K[b,g,j,d]
  *   s_j = c * tanh(s_j / c)                 if a softcap c is given
- *   s_j = s_j + slope[h] * (j - qi)         if ALiBi slopes are given
+ *   s_j = s_j + slope[h] * (j - i)          if ALiBi slopes are given
  *   s_j = -inf                              if position j is not admissible
  *
+ * where i = qpos0 + qi is the query row's position among the keys: qpos0 = 0
+ * is the top-left alignment of position_admissible (row qi at position qi);
+ * a decode row, the newest token of its sequence, sits at qpos0 = Sk - 1
+ * ("gfx942 unified attention", section 4: bottom-right alignment, under which
+ * a single non-causal query row is the causal one).
+ *
  * admissible (attention.fkc.md, header: position_admissible):
- *   not (causal and j > qi), not (left window and j + left < qi),
- *   not (right window and j > qi + right); plus an optional per-row inclusive
- *   key range [lo, hi] (row_bounds, [B, Sq, 2]) -- the reading used for rows
- *   "given a window that masks all keys".
+ *   not (causal and j > i), not (left window and j + left < i),
+ *   not (right window and j > i + right); plus an optional per-row inclusive
+ *   key range [lo, hi] (row_bounds, [B, Sq, 2], indexed by the row qi) -- the
+ *   reading used for rows "given a window that masks all keys".
  *
  * Then the stable softmax of section 2 of "gfx942 unified attention, from the
  * math up": M = max_j s_j, w_j = exp(s_j - M), L = sum_j w_j,
@@ -84,13 +90,15 @@ typedef struct {
     int causal;
     long wl, wr;
     double softcap;
+    long qpos0; /* position of query row 0 */
 } problem;
 
 /* position_admissible plus the optional per-row range. */
 static int admissible(const problem *p, int b, int qi, int kj) {
-    if (p->causal && kj > qi) return 0;
-    if (p->wl >= 0 && (long)kj + p->wl < (long)qi) return 0;
-    if (p->wr >= 0 && (long)kj > (long)qi + p->wr) return 0;
+    const long i = p->qpos0 + qi;
+    if (p->causal && (long)kj > i) return 0;
+    if (p->wl >= 0 && (long)kj + p->wl < i) return 0;
+    if (p->wr >= 0 && (long)kj > i + p->wr) return 0;
     if (p->row_bounds) {
         const int32_t *rb = p->row_bounds + 2 * ((int64_t)b * p->Sq + qi);
         if (kj < rb[0] || kj > rb[1]) return 0;
@@ -108,7 +116,7 @@ static double score(const problem *p, int b, int h, int qi, int kj) {
         dot += widen(p->dtype, p->q, qoff + d) * widen(p->dtype, p->k, koff + d);
     double s = p->scale * dot;
     if (p->softcap > 0.0) s = p->softcap * tanh(s / p->softcap);
-    if (p->slopes) s += (double)p->slopes[h] * (double)(kj - qi);
+    if (p->slopes) s += (double)p->slopes[h] * (double)((long)kj - (p->qpos0 + qi));
     return s;
 }
 
@@ -148,16 +156,17 @@ static int check(const problem *p) {
  * Materialised oracle.  rows == NULL computes every (b, h, qi) and writes
  * out[((b*Hq + h)*Sq + qi)*D + d]; otherwise it computes only the nrows flat
  * row indices rows[i] = (b*Hq + h)*Sq + qi and writes out[i*D + d].
- * lse (nullable) follows the same indexing without the D factor.
+ * lse (nullable) follows the same indexing without the D factor.  Query row
+ * qi sits at position qpos0 + qi.
  */
 int oracle_attn_rows(int dtype, const void *q, const void *k, const void *v,
                      const float *slopes, const int32_t *row_bounds,
                      int B, int Hq, int Hkv, int Sq, int Sk, int D,
                      double scale, int causal, long wl, long wr, double softcap,
-                     const int64_t *rows, int64_t nrows, double *out, double *lse,
+                     long qpos0, const int64_t *rows, int64_t nrows, double *out, double *lse,
                      int nthreads) {
     problem p = {dtype, q, k, v, slopes, row_bounds, B, Hq, Hkv, Sq, Sk, D,
-                 scale, causal, wl, wr, softcap};
+                 scale, causal, wl, wr, softcap, qpos0};
     if (check(&p)) return -1;
     int64_t total = rows ? nrows : (int64_t)B * Hq * Sq;
 #ifdef _OPENMP
@@ -193,7 +202,7 @@ int oracle_attn_tiled(int dtype, const void *q, const void *k, const void *v,
                       double scale, int causal, long wl, long wr, double softcap,
                       int BR, int BC, double *out, double *lse, int nthreads) {
     problem p = {dtype, q, k, v, slopes, row_bounds, B, Hq, Hkv, Sq, Sk, D,
-                 scale, causal, wl, wr, softcap};
+                 scale, causal, wl, wr, softcap, 0};
     if (check(&p) || BR <= 0 || BC <= 0) return -1;
     int nqt = (Sq + BR - 1) / BR;
     int64_t units = (int64_t)B * Hq * nqt;

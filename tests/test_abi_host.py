@@ -73,7 +73,9 @@ def test_forward_rejects_bad_arguments(L, kw, status):
 
 def test_decode_rejects_bad_arguments(L):
     P = ctypes.c_void_p
-    base = [P(FAKE), P(FAKE * 2), P(FAKE * 3), None, P(FAKE * 4), None, 2, 4, 2, 128, 128, 0.1, 0.0, 0,
+    # q, k, v, slopes, out, lse, B, Hq, Hkv, Sk, D, scale, softcap, window_left, window_right,
+    # splits, ws, ws_bytes, dtype, stream
+    base = [P(FAKE), P(FAKE * 2), P(FAKE * 3), None, P(FAKE * 4), None, 2, 4, 2, 128, 128, 0.1, 0.0, -1, -1, 0,
             None, 0, 0, None]
     def call(i, val):
         a = list(base)
@@ -82,8 +84,10 @@ def test_decode_rejects_bad_arguments(L):
     assert call(6, 0) == 1          # B = 0
     assert call(8, 3) == 1          # Hq % Hkv
     assert call(10, 96) == 2        # D
-    assert call(16, 1) == 2         # fp32 decode not built
-    assert call(13, -1) == 1        # negative split count
+    assert call(18, 1) == 2         # fp32 decode not built
+    assert call(15, -1) == 1        # negative split count
+    assert call(13, -2) == 1        # window_left below -1
+    assert call(14, -3) == 1        # window_right below -1
     assert L.attn_decode_workspace_size(0, 4, 2, 128, 128, 0) == 0
     assert L.attn_decode_workspace_size(2, 4, 2, 8192, 128, 1) == 0
     n = L.attn_decode_workspace_size(2, 4, 2, 8192, 128, 4)
@@ -112,9 +116,10 @@ def test_binding_refuses_cpu_tensors():
 def test_paged_decode_rejects_bad_arguments(L):
     P = ctypes.c_void_p
     # q, k_cache, v_cache, block_table, context_lens, slopes, out, lse,
-    # B, Hq, Hkv, D, num_blocks, block_size, max_blocks, scale, softcap, splits, ws, ws_bytes, dtype, stream
+    # B, Hq, Hkv, D, num_blocks, block_size, max_blocks, scale, softcap, window_left, window_right,
+    # splits, ws, ws_bytes, dtype, stream
     base = [P(FAKE), P(FAKE * 2), P(FAKE * 3), P(FAKE * 5), P(FAKE * 6), None, P(FAKE * 4), None,
-            2, 4, 2, 128, 10, 64, 4, 0.1, 0.0, 1, None, 0, 0, None]
+            2, 4, 2, 128, 10, 64, 4, 0.1, 0.0, -1, -1, 1, None, 0, 0, None]
     def call(i, val):
         a = list(base)
         a[i] = val
@@ -126,8 +131,10 @@ def test_paged_decode_rejects_bad_arguments(L):
     assert call(3, None) == 1         # no block table
     assert call(4, P(FAKE * 6 + 2)) == 1  # misaligned context lengths
     assert call(11, 96) == 2          # D
-    assert call(20, 1) == 2           # fp32 not built
-    assert call(20, 3) == 1           # no such type
+    assert call(22, 1) == 2           # fp32 not built
+    assert call(22, 3) == 1           # no such type
+    assert call(17, -2) == 1          # window_left below -1
+    assert call(18, -2) == 1          # window_right below -1
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 48, 128, 0) == 0
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 1) == 0
     assert L.attn_decode_paged_workspace_size(2, 4, 2, 4, 64, 128, 2) == \

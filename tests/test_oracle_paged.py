@@ -30,19 +30,19 @@ def _identity_table(B, Sk, bs):
 @pytest.mark.parametrize("cap,alibi", [(None, False), (30.0, False), (None, True), (20.0, True)])
 def test_identity_table_equals_contiguous_decode(bs, cap, alibi):
     """With blocks laid out in order and context = Sk, paged decode is the
-    contiguous decode: outputs agree; lse differs only by the ALiBi constant,
-    slope_h * (Sk - 1), since the contiguous decode puts its query at 0 and the
-    paged one at abs_pos = Sk - 1."""
+    contiguous decode: both put the query at position Sk - 1, so outputs and
+    lse agree (the paged oracle is torch float64 code, the contiguous decode
+    the C oracle)."""
     B, Hq, Hkv, Sk, D = 2, 4, 2, 128, 16
     q, k, v = _rand((B, Hq, 1, D), 0), _rand((B, Hkv, Sk, D), 1), _rand((B, Hkv, Sk, D), 2)
     slopes = synth.alibi_slopes(Hq) if alibi else None
-    ref, ref_lse = oracle.decode(q, k, v, softcap=cap, alibi_slopes=slopes, return_lse=True)
-    out, lse = oracle.attn_paged(q, _identity_pool(k, bs), _identity_pool(v, bs), _identity_table(B, Sk, bs),
-                                 torch.full((B,), Sk, dtype=torch.int32), softcap=cap, alibi_slopes=slopes,
-                                 return_lse=True)
-    assert (out - ref).abs().max().item() < 1e-12
-    shift = torch.zeros(Hq, dtype=torch.float64) if slopes is None else slopes.double() * (Sk - 1)
-    assert (lse - (ref_lse - shift[None, :, None])).abs().max().item() < 1e-10
+    for wl in (None, 0, 37, 200):
+        ref, ref_lse = oracle.decode(q, k, v, softcap=cap, alibi_slopes=slopes, window_left=wl, return_lse=True)
+        out, lse = oracle.attn_paged(q, _identity_pool(k, bs), _identity_pool(v, bs), _identity_table(B, Sk, bs),
+                                     torch.full((B,), Sk, dtype=torch.int32), softcap=cap, alibi_slopes=slopes,
+                                     window_left=wl, return_lse=True)
+        assert (out - ref).abs().max().item() < 1e-12
+        assert (lse - ref_lse).abs().max().item() < 1e-10
 
 
 def test_implicit_causal_is_bottom_right_causal():

@@ -86,13 +86,13 @@ def lib() -> ctypes.CDLL:
             L.attn_fwd_ex.restype = I
             L.attn_decode_workspace_size.argtypes = [I, I, I, I, I, I]
             L.attn_decode_workspace_size.restype = Z
-            L.attn_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, F, I, P, Z, I, P]
+            L.attn_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, F, F, I, I, I, P, Z, I, P]
             L.attn_decode.restype = I
             L.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, I, F, I, P]
             L.attn_fwd_varlen.restype = I
             L.attn_decode_paged_workspace_size.argtypes = [I, I, I, I, I, I, I]
             L.attn_decode_paged_workspace_size.restype = Z
-            L.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, P, Z, I, P]
+            L.attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, I, P, Z, I, P]
             L.attn_decode_paged.restype = I
             L.attn_bwd_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
             L.attn_bwd_workspace_size.restype = Z
@@ -201,9 +201,12 @@ def decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits=0) -> int:
     return int(lib().attn_decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits))
 
 
-def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None, num_splits=0, out=None,
-                lse=None, workspace=None, stream=None):
+def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None, window_left=None,
+                window_right=None, num_splits=0, out=None, lse=None, workspace=None, stream=None):
     """Split-KV decode.  q [B,Hq,1,D], k/v [B,Hkv,Sk,D] bf16 or fp16 (CUDA).
+
+    The query is the newest token, at position Sk - 1: ALiBi adds
+    slope (j - (Sk - 1)); window_left admits keys j >= Sk - 1 - window_left.
 
     workspace: optional uint8 CUDA tensor of at least decode_workspace_size(...)
     bytes; allocated here (through torch) when None.  Returns out [B,Hq,1,D].
@@ -232,8 +235,9 @@ def attn_decode(q, k, v, alibi_slopes=None, *, softmax_scale=None, softcap=None,
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
     st = lib().attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(alibi_slopes), _ptr(out), _ptr(lse),
-                           B, Hq, Hkv, Sk, D, scale, float(softcap or 0.0), int(num_splits),
-                           _ptr(workspace), ws_bytes, _DT16[q.dtype], _stream_handle(stream))
+                           B, Hq, Hkv, Sk, D, scale, float(softcap or 0.0), _win(window_left),
+                           _win(window_right), int(num_splits), _ptr(workspace), ws_bytes, _DT16[q.dtype],
+                           _stream_handle(stream))
     if st:
         raise GbattnError(st, "attn_decode")
     return out
@@ -284,7 +288,8 @@ def decode_paged_workspace_size(B, Hq, Hkv, max_blocks_per_seq, block_size, D, n
 
 
 def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slopes=None, *, softmax_scale=None,
-                      softcap=None, num_splits=0, out=None, lse=None, workspace=None, stream=None):
+                      softcap=None, window_left=None, window_right=None, num_splits=0, out=None, lse=None,
+                      workspace=None, stream=None):
     """Decode over a paged KV cache (see attn_decode_paged in gbattn.h).
 
     q [B,Hq,1,D] bf16 or fp16; k_cache / v_cache [num_blocks, block_size, Hkv, D] of the same type;
@@ -324,8 +329,9 @@ def attn_decode_paged(q, k_cache, v_cache, block_table, context_lens, alibi_slop
     scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
     st = lib().attn_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(context_lens),
                                  _ptr(alibi_slopes), _ptr(out), _ptr(lse), B, Hq, Hkv, D, num_blocks, block_size,
-                                 max_blocks, scale, float(softcap or 0.0), int(num_splits), _ptr(workspace),
-                                 ws_bytes, _DT16[q.dtype], _stream_handle(stream))
+                                 max_blocks, scale, float(softcap or 0.0), _win(window_left), _win(window_right),
+                                 int(num_splits), _ptr(workspace), ws_bytes, _DT16[q.dtype],
+                                 _stream_handle(stream))
     if st:
         raise GbattnError(st, "attn_decode_paged")
     return out

@@ -494,6 +494,24 @@ static int decode_plan(int B, int Hq, int Hkv, int Sk, int D, int num_splits, in
     return 0;
 }
 
+// Split plan of a decode whose query admits only the keys of a left window
+// (window_left >= 0): the plan over the 64-key tiles such a window can touch,
+// with no more splits than the plan over all Sk keys, which sizes the
+// caller's workspace.
+static void decode_plan_window(int B, int Hkv, int Sk, int wl, int sms, int requested, int* splits, int* chunk) {
+    decode_split_plan(B, Hkv, Sk, sms, requested, splits, chunk);
+    if (wl < 0) return;
+    const long long keys = wl + 1LL < (long long)Sk ? wl + 1LL : (long long)Sk;  // admitted keys, at most
+    const long long all_tiles = (Sk + 63LL) / 64;
+    const long long span = (keys + 62) / 64 + 1;  // 64-key tiles a range of `keys` keys can touch
+    if (span >= all_tiles) return;
+    int s2 = 0, c2 = 0;
+    decode_split_plan(B, Hkv, (int)(span * 64), sms, requested, &s2, &c2);
+    if (s2 > *splits) decode_split_plan(B, Hkv, (int)(span * 64), sms, *splits, &s2, &c2);
+    *splits = s2;
+    *chunk = c2;
+}
+
 size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Sk, int D, int num_splits) {
     int splits = 0, chunk = 0;
     if (decode_plan(B, Hq, Hkv, Sk, D, num_splits, &splits, &chunk)) return 0;
@@ -504,12 +522,13 @@ size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Sk, int D, int num
 }
 
 int attn_decode(const void* q, const void* k, const void* v, const float* alibi_slopes, void* out, float* lse_out,
-                int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap, int num_splits,
-                void* workspace, size_t workspace_bytes, int dtype, void* stream) {
+                int B, int Hq, int Hkv, int Sk, int D, float softmax_scale, float softcap, int window_left,
+                int window_right, int num_splits, void* workspace, size_t workspace_bytes, int dtype, void* stream) {
     int rc = check_common(B, Hq, Hkv, 1, Sk, D, softmax_scale, softcap, dtype);
     if (rc) return rc;
     if (dtype == GBATTN_F32) return GBATTN_ERR_UNSUPPORTED;
     if (!q || !k || !v || !out || num_splits < 0) return GBATTN_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return GBATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return GBATTN_ERR_INVALID_ARG;
     if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u)) return GBATTN_ERR_INVALID_ARG;
     if (alibi_slopes && (reinterpret_cast<uintptr_t>(alibi_slopes) & 3u)) return GBATTN_ERR_INVALID_ARG;
@@ -519,8 +538,10 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
 
     DecodeProblem f{};
     if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
-    decode_split_plan(B, Hkv, Sk, f.num_sms, num_splits, &f.num_splits, &f.chunk);
-    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, Sk, D, num_splits);
+    decode_plan_window(B, Hkv, Sk, window_left, f.num_sms, num_splits, &f.num_splits, &f.chunk);
+    const size_t need = f.num_splits > 1 ? (size_t)B * Hq * f.num_splits * D * 4 +
+                                               (((size_t)B * Hq * f.num_splits * 4 + 15) & ~size_t(15))
+                                         : 0;
     if (need > 0) {
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GBATTN_ERR_INVALID_ARG;
         if (overlaps(workspace, need, out, nq) || overlaps(workspace, need, q, nq) ||
@@ -542,6 +563,7 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
     f.D = D;
     f.scale = softmax_scale;
     f.softcap = softcap;
+    f.wl = window_left;
     f.timeout_ns = g_timeout_ns;
     f.f16 = dtype == GBATTN_F16;
     CUtensorMap tk, tv;
@@ -571,8 +593,8 @@ size_t attn_decode_paged_workspace_size(int B, int Hq, int Hkv, int max_blocks_p
 int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, const uint32_t* block_table,
                       const uint32_t* context_lens, const float* alibi_slopes, void* out, float* lse_out, int B,
                       int Hq, int Hkv, int D, int num_blocks, int block_size, int max_blocks_per_seq,
-                      float softmax_scale, float softcap, int num_splits, void* workspace, size_t workspace_bytes,
-                      int dtype, void* stream) {
+                      float softmax_scale, float softcap, int window_left, int window_right, int num_splits,
+                      void* workspace, size_t workspace_bytes, int dtype, void* stream) {
     int max_ctx = 0;
     if (!paged_geometry(block_size, max_blocks_per_seq, num_blocks, &max_ctx)) return GBATTN_ERR_INVALID_ARG;
     int rc = check_common(B, Hq, Hkv, 1, max_ctx, D, softmax_scale, softcap, dtype);
@@ -580,6 +602,7 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
     if (dtype == GBATTN_F32) return GBATTN_ERR_UNSUPPORTED;
     if (!q || !k_cache || !v_cache || !block_table || !context_lens || !out || num_splits < 0)
         return GBATTN_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return GBATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return GBATTN_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(context_lens)) & 3u)
         return GBATTN_ERR_INVALID_ARG;
@@ -591,8 +614,10 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
 
     DecodeProblem f{};
     if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
-    decode_split_plan(B, Hkv, max_ctx, f.num_sms, num_splits, &f.num_splits, &f.chunk);
-    const size_t need = attn_decode_workspace_size(B, Hq, Hkv, max_ctx, D, num_splits);
+    decode_plan_window(B, Hkv, max_ctx, window_left, f.num_sms, num_splits, &f.num_splits, &f.chunk);
+    const size_t need = f.num_splits > 1 ? (size_t)B * Hq * f.num_splits * D * 4 +
+                                               (((size_t)B * Hq * f.num_splits * 4 + 15) & ~size_t(15))
+                                         : 0;
     if (need > 0) {
         if (!workspace || workspace_bytes < need || !aligned16(workspace)) return GBATTN_ERR_INVALID_ARG;
         if (overlaps(workspace, need, out, nq) || overlaps(workspace, need, q, nq) ||
@@ -614,6 +639,7 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
     f.D = D;
     f.scale = softmax_scale;
     f.softcap = softcap;
+    f.wl = window_left;
     f.timeout_ns = g_timeout_ns;
     f.paged = 1;
     f.block_table = block_table;

@@ -55,6 +55,7 @@ struct DecParams {
     int n_tiles;        // tiles over Sk
     float qscale;       // multiplies q: scale * log2(e) (no softcap) or scale (softcap)
     float softcap;
+    int wl;             // left window (-1: none): keys j >= len - 1 - wl
     // paged cache: tile t of sequence b gathers keys [64 t, 64 t + 64) block by block
     const uint32_t* block_table;   // [B, max_blocks]
     const uint32_t* context_lens;  // [B]
@@ -116,15 +117,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     const int hkv = rem % p.Hkv;
     const int b = rem / p.Hkv;
     // Keys of this sequence: all Sk, or (paged cache) its context length,
-    // capped at what the block table can hold.  The query's absolute position
-    // for ALiBi is 0 (contiguous) or len - 1 (paged: the last position).
+    // capped at what the block table can hold.  The query is the newest token,
+    // at position len - 1: the ALiBi term is slope (j - (len - 1)) and a left
+    // window admits keys j >= len - 1 - wl.  The splits cover the 64-key tiles
+    // from the window's first key to the last key.
     int len = p.Sk;
     if (PAGED) {
         const uint32_t c = __ldg(p.context_lens + b);
         len = c > (uint32_t)p.Sk ? p.Sk : (int)c;
         if (c > (uint32_t)p.Sk && threadIdx.x == 0 && split == 0 && hc == 0) atomicOr(p.status, ST_DECODE_PAGED_RANGE);
     }
-    const int t_begin = split * p.chunk_tiles;
+    const int k_first = p.wl >= 0 ? max(0, len - 1 - p.wl) : 0;  // first admitted key
+    const int t_begin = k_first / TILE + split * p.chunk_tiles;
     const int t_end = min(PAGED ? (len + TILE - 1) / TILE : p.n_tiles, t_begin + p.chunk_tiles);
     const int h0 = hkv * p.G + hc * GC;                     // first query head of this chunk
     const int n_heads = min(GC, p.G - hc * GC);
@@ -302,8 +306,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
                 const float e = ex2_approx(x * (2.f * LOG2E / p.softcap));
                 x = p.softcap * LOG2E * (1.f - 2.f / (e + 1.f));
             }
-            if (ALIBI) x = fmaf(slope_l2, (float)(PAGED ? kj - (len - 1) : kj), x);
-            if (kj >= len) x = -INFINITY;
+            if (ALIBI) x = fmaf(slope_l2, (float)(kj - (len - 1)), x);
+            if (kj >= len || kj < k_first) x = -INFINITY;
             sv[ps] = x;
             mt = fmaxf(mt, x);
         }
@@ -517,6 +521,7 @@ cudaError_t launch_decode_bf16(const DecodeProblem& f, const CUtensorMap& tk, co
     p.Sk = f.Sk;
     p.G = f.Hq / f.Hkv;
     p.num_splits = f.num_splits;
+    p.wl = f.wl;
     p.chunk_tiles = f.chunk / TILE;
     p.n_tiles = (f.Sk + TILE - 1) / TILE;
     p.softcap = f.softcap;

@@ -56,6 +56,6 @@ extern "C" int attn_decode_noalloc(const void* q, const void* k, const void* v, 
     void* scratch = nullptr;
     const int rc = scratch_address(&scratch);
     if (rc != GBATTN_OK) return rc;
-    return attn_decode(q, k, v, alibi_slopes, out, lse_out, B, Hq, Hkv, Sk, D, softmax_scale, softcap, num_splits,
-                       scratch, (size_t)GBATTN_NOALLOC_SCRATCH_BYTES, dtype, stream);
+    return attn_decode(q, k, v, alibi_slopes, out, lse_out, B, Hq, Hkv, Sk, D, softmax_scale, softcap, -1, -1,
+                       num_splits, scratch, (size_t)GBATTN_NOALLOC_SCRATCH_BYTES, dtype, stream);
 }

@@ -45,6 +45,7 @@ struct DecodeProblem {
     int B, Hq, Hkv, Sk, D;
     float scale;
     float softcap;
+    int wl;                     // left window at the query's position (the last key); -1 = none
     int num_splits;             // resolved (>= 1)
     int chunk;                  // keys per split, multiple of 64
     float* ws_o;                // [B, Hq, num_splits, D] fp32 (num_splits > 1)
