@@ -238,6 +238,21 @@ __device__ __forceinline__ bool decode_item(const Params& p, int item, Slot (&s)
     return s[0].t >= 0 || s[1].t >= 0;
 }
 
+// Column indices (j, j + 1) of the key pairs of a tile, for the packed ALiBi bias.
+__constant__ float2 c_key_pairs[BN / 2] = {
+#define GBATTN_KP(i) {2.f * (i), 2.f * (i) + 1.f}
+    GBATTN_KP(0),  GBATTN_KP(1),  GBATTN_KP(2),  GBATTN_KP(3),  GBATTN_KP(4),  GBATTN_KP(5),  GBATTN_KP(6),
+    GBATTN_KP(7),  GBATTN_KP(8),  GBATTN_KP(9),  GBATTN_KP(10), GBATTN_KP(11), GBATTN_KP(12), GBATTN_KP(13),
+    GBATTN_KP(14), GBATTN_KP(15), GBATTN_KP(16), GBATTN_KP(17), GBATTN_KP(18), GBATTN_KP(19), GBATTN_KP(20),
+    GBATTN_KP(21), GBATTN_KP(22), GBATTN_KP(23), GBATTN_KP(24), GBATTN_KP(25), GBATTN_KP(26), GBATTN_KP(27),
+    GBATTN_KP(28), GBATTN_KP(29), GBATTN_KP(30), GBATTN_KP(31), GBATTN_KP(32), GBATTN_KP(33), GBATTN_KP(34),
+    GBATTN_KP(35), GBATTN_KP(36), GBATTN_KP(37), GBATTN_KP(38), GBATTN_KP(39), GBATTN_KP(40), GBATTN_KP(41),
+    GBATTN_KP(42), GBATTN_KP(43), GBATTN_KP(44), GBATTN_KP(45), GBATTN_KP(46), GBATTN_KP(47), GBATTN_KP(48),
+    GBATTN_KP(49), GBATTN_KP(50), GBATTN_KP(51), GBATTN_KP(52), GBATTN_KP(53), GBATTN_KP(54), GBATTN_KP(55),
+    GBATTN_KP(56), GBATTN_KP(57), GBATTN_KP(58), GBATTN_KP(59), GBATTN_KP(60), GBATTN_KP(61), GBATTN_KP(62),
+    GBATTN_KP(63)};
+#undef GBATTN_KP
+
 __device__ __forceinline__ int item_of(int k, int cta, int grid) {
     return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
 }
@@ -325,7 +340,11 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
         if (i_row < seq_q_len<VARLEN>(p, sl)) row_interval<VARLEN>(p, sl, i_row, ra, rb);
         float slope_l2 = 0.f;
         if (ALIBI) slope_l2 = __ldg(p.slopes + sl.h) * LOG2E;
-        float m_used = -INFINITY, l = 0.f;
+        // A row with no admissible key (or past the sequence) takes +inf as its
+        // reference max: every p of the row is then exactly 0 (l = 0, O = 0)
+        // without masking its elements on each tile.
+        const bool row_live = ra <= rb;
+        float m_used = row_live ? -INFINITY : INFINITY, l = 0.f;
         constexpr bool DOWN = ALIBI;
         for (int u = first_tile<DOWN>(sl);; u += DOWN ? -1 : 1) {
             if (DOWN ? u < sl.lo : u > sl.hi) break;
@@ -343,26 +362,33 @@ __device__ __forceinline__ void softmax_role(const Params& p, Smem& sm, uint32_t
                 // tanh is the hardware approximation (relative error about 2^-11,
                 // far below the bf16 rounding of P); the ALiBi bias of key k0 + j is
                 // base + slope * j with one conversion per tile.
+                // Column pairs go through packed FP32 operations; the bias of keys
+                // (j, j + 1) is one FFMA2 against their indices in constant memory.
                 const float abase = ALIBI ? slope_l2 * (float)(k0 - qi) : 0.f;
+                const float2 ab2 = make_float2(abase, abase), sl2b = make_float2(slope_l2, slope_l2);
+                const float2 ci2 = make_float2(p.cap_in, p.cap_in), co2 = make_float2(p.cap_out, p.cap_out);
 #pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    float t;
+                for (int j = 0; j < BN; j += 2) {
+                    float2 t = make_float2(sv[j], sv[j + 1]);
                     if (SOFTCAP) {
-                        t = p.cap_out * tanh_approx(sv[j] * p.cap_in);
+                        t = __fmul2_rn(t, ci2);
+                        t = make_float2(tanh_approx(t.x), tanh_approx(t.y));
+                        t = ALIBI ? __ffma2_rn(t, co2, __ffma2_rn(sl2b, c_key_pairs[j >> 1], ab2)) : __fmul2_rn(t, co2);
                     } else {
-                        t = sv[j] * p.scale_log2;
+                        t = __ffma2_rn(t, sl2, __ffma2_rn(sl2b, c_key_pairs[j >> 1], ab2));
                     }
-                    if (ALIBI) t += fmaf(slope_l2, (float)j, abase);
-                    sv[j] = t;
+                    sv[j] = t.x;
+                    sv[j + 1] = t.y;
                 }
             }
-            // admissible keys of the tile: lo <= j <= hi (none when lo > hi);
-            // with no lower bound in the tile for any row of the warp (causal
-            // masks) one compare per key suffices.  The vote is taken by the
-            // whole warp, before the per-row branch.
+            // admissible keys of the tile: lo <= j <= hi; rows with none are
+            // not masked (their reference max is +inf).  With no lower bound in
+            // the tile for any live row of the warp (causal masks) one compare
+            // per key suffices.  The vote is taken by the whole warp, before the
+            // per-row branch.
             const int lo = ra - k0, hi = rb - k0;
-            const bool no_lower = __all_sync(0xffffffffu, lo <= 0);
-            if (k0 < ra || k0 + BN - 1 > rb) {
+            const bool no_lower = __all_sync(0xffffffffu, !row_live || lo <= 0);
+            if (row_live && (k0 < ra || k0 + BN - 1 > rb)) {
                 if (no_lower) {
 #pragma unroll
                     for (int j = 0; j < BN; ++j) sv[j] = (j > hi) ? -INFINITY : sv[j];
