@@ -93,10 +93,10 @@ def test_bf16_flags(cuda_device, D, flags):
 
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("softcap", [21.0, 23.0, 25.0])
-def test_bf16_softcap_near_the_polynomial_range(cuda_device, D, softcap):
-    # Scores scale * q.k are about N(0, 1) and reach 4 to 5 in a 128 x 128 tile,
-    # so |scale s / softcap| of a tile lands on both sides of 0.2: some tiles
-    # take the cubic softcap, others the hardware tanh.
+def test_bf16_softcap_moderate_caps(cuda_device, D, softcap):
+    # Scores scale * q.k are about N(0, 1) and reach 4 to 5 in a 128 x 128 tile:
+    # caps of 21..25 bend the largest scores by a few percent, with and without
+    # ALiBi and windows.
     run_case(cuda_device, 2, 4, 2, 520, 520, D, causal=True, softcap=softcap)
     run_case(cuda_device, 1, 4, 4, 300, 300, D, softcap=softcap, alibi=True, wl=200, wr=50)
 
