@@ -84,3 +84,25 @@ def test_decode_workload(cuda_device):
         ref, ref_lse = oracle.decode(q, k, v, scale=w.scale, return_lse=True)
         check_out(out[b:b + 1, h:h + 1], ref, torch.bfloat16, f"decode row {r}")
         check_lse(lse[b:b + 1, h:h + 1].reshape(1, 1, 1), ref_lse, torch.bfloat16, f"decode row {r}")
+
+
+@pytest.mark.parametrize("shape", [(8, 16, 8, 4096, 128), (16, 8, 8, 4096, 64)], ids=["gqa2_d128", "mha_d64"])
+def test_dense_prefill_with_kv_beyond_l2(cuda_device, shape):
+    """Dense problems whose K and V (134 MB here) do not fit in L2: more work
+    items than one pass of the persistent grid, both GQA pairings; sampled rows
+    against the oracle."""
+    import tiled_scaled_dot_gb300 as g
+    from synth.workloads import scaled
+    B, Hq, Hkv, S, D = shape
+    w = scaled(WORKLOADS["bf16_causal_b4_h32_s2048_d128"], name=f"banded_{B}_{Hq}_{Hkv}_{S}_{D}", B=B, Hq=Hq,
+               Hkv=Hkv, Sq=S, Sk=S, D=D)
+    assert 2 * B * Hkv * S * D * 2 > 64 * 2**20
+    x = make_inputs(w, cuda_device)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=cuda_device)
+    out = g.attn_fwd(x["q"], x["k"], x["v"], causal=True, lse=lse)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    rows = _sample_rows(w, None, n=256)
+    ref, ref_lse = oracle.attn(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), causal=True, rows=rows, return_lse=True)
+    check_out(out.view(-1, D)[rows.to(cuda_device)], ref, torch.bfloat16, w.name)
+    check_lse(lse.view(-1)[rows.to(cuda_device)], ref_lse, torch.bfloat16, w.name)

@@ -77,6 +77,13 @@ constexpr int NG = 8;
 // releases an entry after copying it.
 constexpr int NI = 4;
 constexpr int ITEM_READERS = 32 + 2 * 128 + 128;
+// K + V bytes of the packed sequences whose items run together: about a fifth
+// of the 126 MB L2, so that a band's K and V survive the Q and O streams that
+// pass through L2 between two reads of the same key tile (on GB300, 24 MB bands
+// beat 16 and 48 MB ones on packed-sequence prefill).  Dense problems run as
+// one band: banding them measured 5-7 % slower (heaviest-first over the whole
+// list balances the SMs better, and their K / V re-reads cost little time).
+constexpr double L2_BAND_BYTES = 24.0 * 1024 * 1024;
 
 template <int D>
 struct Cfg {
@@ -113,6 +120,7 @@ struct Params {
     float cap_out;     // softcap * log2(e)
     int n_qt;          // query tiles per head (packed sequences: per sequence, at most)
     int pair_heads;    // 1: slots are heads (2p, 2p+1) at one row tile; 0: row tiles (2t, 2t+1) of one head
+    int band;          // sequences per band: work items run band by band (all of B for dense problems)
     int n_items;
     // Packed variable-length sequences ("gfx942 unified attention", sections
     // 4-5): q / out [total_q, Hq, D], k / v [total_k, Hkv, D]; sequence b's
@@ -168,21 +176,23 @@ __device__ __forceinline__ void row_interval(const Params& p, const Slot& s, int
 template <bool VARLEN>
 __device__ __forceinline__ bool decode_item(const Params& p, int item, Slot (&s)[2]) {
     const int lane = threadIdx.x & 31;
+    // Items run band by band (p.band sequences each, so a band's K and V stay
+    // in L2 while its items run), heaviest row tiles first within a band.
+    const int hp = p.pair_heads ? p.Hq / 2 : p.Hq;         // slot pairs per (sequence, row rank)
+    const int n_r = p.pair_heads ? p.n_qt : (p.n_qt + 1) / 2;  // row ranks
+    const int per_band = n_r * p.band * hp;
+    const int band = item / per_band, w = item % per_band;
+    const int tr = w / (p.band * hp), rest = w % (p.band * hp);
+    const int b = band * p.band + rest / hp, pr = rest % hp;
+    if (b >= p.B) return false;
     if (p.pair_heads) {
-        const int per_t = p.B * (p.Hq / 2);
-        int tr = item / per_t, rest = item % per_t;
         int t = p.causal ? (p.n_qt - 1 - tr) : tr;
-        int b = rest / (p.Hq / 2), pr = rest % (p.Hq / 2);
         s[0] = Slot{b, 2 * pr, t, 0, -1, 0, p.Sq, 0, p.Sk};
         s[1] = Slot{b, 2 * pr + 1, t, 0, -1, 0, p.Sq, 0, p.Sk};
     } else {
-        const int n_tp = (p.n_qt + 1) / 2;
-        const int per_t = p.B * p.Hq;
-        int tr = item / per_t, rest = item % per_t;
-        int tp = p.causal ? (n_tp - 1 - tr) : tr;
-        int b = rest / p.Hq, h = rest % p.Hq;
-        s[0] = Slot{b, h, 2 * tp, 0, -1, 0, p.Sq, 0, p.Sk};
-        s[1] = Slot{b, h, (2 * tp + 1 < p.n_qt) ? 2 * tp + 1 : -1, 0, -1, 0, p.Sq, 0, p.Sk};
+        int tp = p.causal ? (n_r - 1 - tr) : tr;
+        s[0] = Slot{b, pr, 2 * tp, 0, -1, 0, p.Sq, 0, p.Sk};
+        s[1] = Slot{b, pr, (2 * tp + 1 < p.n_qt) ? 2 * tp + 1 : -1, 0, -1, 0, p.Sq, 0, p.Sk};
     }
     if (VARLEN) {
         // the sequence's rows; offsets or lengths outside the tensors are
@@ -632,6 +642,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tma_prefetch_desc(&tmV);
             }
             uint32_t ld_cnt = 0, grp_cnt = 0, q_cnt[2] = {0, 0};
+            // L2 policies of packed sequences: Q read once, K / V read again by the band's other items
+            const uint64_t pol_first = createpolicy_evict_first(), pol_last = createpolicy_evict_last();
             int slot_grp[C::NS];  // group that last filled each slot (-1: none)
 #pragma unroll
             for (int i = 0; i < C::NS; ++i) slot_grp[i] = -1;
@@ -672,9 +684,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_expect_tx(&sm.q_full[x], C::Q_BYTES);
 #pragma unroll
                         for (int hf = 0; hf < C::HALVES; ++hf) {
-                            if (VARLEN)  // packed [total_q][Hq][D]
-                                tma_load_3d(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].h,
-                                            s[x].q0 + s[x].t * BM);
+                            if (VARLEN)  // packed [total_q][Hq][D]; each Q tile is read once
+                                tma_load_3d_hint(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].h,
+                                                 s[x].q0 + s[x].t * BM, pol_first);
                             else
                                 tma_load_3d(sQ[x] + hf * C::Q_SLAB, &tmQ, &sm.q_full[x], hf * 64, s[x].t * BM,
                                             s[x].b * p.Hq + s[x].h);
@@ -719,9 +731,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             const int key = (is_v ? u : un) * BN;
 #pragma unroll
                             for (int hf = 0; hf < C::HALVES; ++hf) {
-                                if (VARLEN)  // packed [total_k][Hkv][D]
-                                    tma_load_3d(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64, hkv,
-                                                s[0].k0 + key);
+                                if (VARLEN)  // packed [total_k][Hkv][D]; the band's other items read it again
+                                    tma_load_3d_hint(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64, hkv,
+                                                     s[0].k0 + key, pol_last);
                                 else
                                     tma_load_3d(dst + hf * C::KV_SLAB, is_v ? &tmV : &tmK, fb, hf * 64, key,
                                                 s[0].b * p.Hkv + hkv);
@@ -934,10 +946,20 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
     p.total_k = f.total_k;
     p.n_qt = (f.Sq + BM - 1) / BM;
     p.pair_heads = (p.G % 2 == 0) ? 1 : 0;
-    if (p.pair_heads)
-        p.n_items = p.n_qt * f.B * (f.Hq / 2);
-    else
-        p.n_items = ((p.n_qt + 1) / 2) * f.B * f.Hq;
+    // Packed sequences: bands of sequences whose K and V (at the average length)
+    // fill about L2_BAND_BYTES, so that the items running at one time re-read K
+    // and V from L2 rather than DRAM.  Dense problems run as one band.
+    p.band = f.B;
+    if (f.varlen) {
+        const double kv_all = (double)f.total_k * f.Hkv * f.D * 2.0 * 2.0;
+        const double nb = kv_all > 0 ? L2_BAND_BYTES * f.B / kv_all : f.B;
+        p.band = nb < 1.0 ? 1 : (nb > f.B ? f.B : (int)nb);
+    }
+    const long long n_bands = (f.B + p.band - 1) / p.band;
+    const long long n_r = p.pair_heads ? p.n_qt : (p.n_qt + 1) / 2;
+    const long long n_items = n_bands * n_r * p.band * (p.pair_heads ? f.Hq / 2 : f.Hq);
+    if (n_items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    p.n_items = (int)n_items;
     const int grid = p.n_items < f.num_sms ? p.n_items : f.num_sms;
     const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
     // packed sequences are built for bf16 only
