@@ -186,14 +186,15 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch, one-pass ncu
-    # captures of the full-size workloads (values as ncu prints them: three to
-    # five significant figures)
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "a54dfc84dcb7c58b"): 129950000,
-    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "a54dfc84dcb7c58b"): 4105060000,
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "d2740f33f2be2b02"): 2156490000,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "d2740f33f2be2b02"): 1746920000,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "165735717bfcac1f"): 339620000,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "165735717bfcac1f"): 216060000,
+    # captures of the full-size workloads (values as ncu prints them)
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "869b8c2e02d5fd44"): 130418176,
+    ("prefill", "bf16_causal_b1_h32_s8192_d128", "869b8c2e02d5fd44"): 134603776,
+    ("prefill", "bf16_masked_b2_h16_s4096_d64", "869b8c2e02d5fd44"): 51266560,
+    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "869b8c2e02d5fd44"): 1778597888,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "20cc43071f094d9e"): 2155364096,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "20cc43071f094d9e"): 1749039616,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "889136898a718355"): 341057536,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "889136898a718355"): 215400960,
 }
 
 
@@ -404,7 +405,9 @@ def bench_decode(g, args, ws, dev, pk):
 
 # What bounds the masked D=64 workload below the tensor roofline (the
 # counters behind it are summarised under profiles/).
-MASKED_LIMITER = None
+MASKED_LIMITER = ("softmax per key tile, not the tensor pipe: each 128-key tile costs a row tanh.approx and "
+                  "ex2.approx per key on MUFU (XU pipe busy 47.9 % of cycles) and about 5 other instructions, "
+                  "against 512 tensor cycles per slot at D = 64 (tensor pipe 17.4 % active; ncu full set)")
 
 
 PAGED_SHAPE = dict(B=64, Hq=32, Hkv=8, D=128, block_size=64, ctx_lo=4096, ctx_hi=8192)
