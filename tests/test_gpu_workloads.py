@@ -106,3 +106,39 @@ def test_dense_prefill_with_kv_beyond_l2(cuda_device, shape):
     ref, ref_lse = oracle.attn(x["q"].cpu(), x["k"].cpu(), x["v"].cpu(), causal=True, rows=rows, return_lse=True)
     check_out(out.view(-1, D)[rows.to(cuda_device)], ref, torch.bfloat16, w.name)
     check_lse(lse.view(-1)[rows.to(cuda_device)], ref_lse, torch.bfloat16, w.name)
+
+
+def test_varlen_bench_workload(cuda_device):
+    """The benchmark's packed workload at full size (32 causal sequences of
+    512..4096 tokens, Hq 32, Hkv 8, D 128: 8 bands of sequences), as the
+    benchmark launches it.  Each checked sequence is compared on sampled rows
+    with the dense oracle over that sequence alone (queries = keys, where the
+    bottom-right causal alignment is the top-left one)."""
+    import tiled_scaled_dot_gb300 as g
+    B, Hq, Hkv, D = 32, 32, 8, 128
+    lens = (512 + synth.randint(B, 4096 - 512 + 1, 0, 7)).tolist()
+    cu = torch.tensor([0] + [sum(lens[:i + 1]) for i in range(B)], dtype=torch.int32)
+    T = int(cu[-1])
+    q = synth.normal((T, Hq, D), 0, synth.STREAM_Q, torch.bfloat16, cuda_device)
+    k = synth.normal((T, Hkv, D), 0, synth.STREAM_K, torch.bfloat16, cuda_device)
+    v = synth.normal((T, Hkv, D), 0, synth.STREAM_V, torch.bfloat16, cuda_device)
+    cud = cu.to(cuda_device)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=cuda_device)
+    out = g.attn_fwd_varlen(q, k, v, cud, cud, max(lens), causal=True, lse=lse)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    order = sorted(range(B), key=lambda i: lens[i])
+    picks = sorted(set([order[0], order[-1]] + synth.randint(4, B, 5, 9).tolist()))
+    for b in picks:
+        a0, n = int(cu[b]), lens[b]
+        qs = q[a0:a0 + n].permute(1, 0, 2).unsqueeze(0).cpu()
+        ks = k[a0:a0 + n].permute(1, 0, 2).unsqueeze(0).cpu()
+        vs = v[a0:a0 + n].permute(1, 0, 2).unsqueeze(0).cpu()
+        w = synth.randint(48, Hq * n, 6, b).tolist()
+        edge = [(h * n + i) for h in (0, Hq - 1) for i in (0, 1, 127, 128, n // 2, n - 129, n - 2, n - 1) if 0 <= i < n]
+        rows = torch.tensor(sorted(set(w + edge)), dtype=torch.int64)
+        ref, ref_lse = oracle.attn(qs, ks, vs, causal=True, rows=rows, return_lse=True)
+        h, i = rows // n, rows % n
+        got = out[a0 + i.to(cuda_device), h.to(cuda_device)]
+        check_out(got, ref, torch.bfloat16, f"varlen bench sequence {b} ({n} tokens)")
+        check_lse(lse[h.to(cuda_device), a0 + i.to(cuda_device)], ref_lse, torch.bfloat16, f"varlen sequence {b}")
