@@ -138,13 +138,15 @@ int attn_fwd_ex(const gbattn_fwd_params* p);
  * slope_h * (j - pos).  Rows with no admissible key are zero (lse -inf).
  * Softcap and scale as in attn_fwd.
  *
- *  q, out         device bf16 [total_q, Hq, D]; k, v device bf16 [total_k, Hkv, D].
+ *  q, out         device [total_q, Hq, D]; k, v device [total_k, Hkv, D]; all of
+ *                 type `dtype`.
  *  cu_seqlens_q, cu_seqlens_k  device int32 [B + 1], non-decreasing, from 0;
  *                 cu_seqlens_q[B] = total_q, cu_seqlens_k[B] <= total_k.
  *  seqused_k      device int32 [B] or NULL.
  *  lse_out        device fp32 [Hq, total_q] (natural log) or NULL.
  *  max_seqlen_q   at least every sequence's query count (sizes the work list).
- *  dtype          GBATTN_BF16 (others return GBATTN_ERR_UNSUPPORTED); D 64 or 128.
+ *  dtype          GBATTN_BF16 or GBATTN_F16 (tensor cores, fp32 accumulation;
+ *                 GBATTN_F32 returns GBATTN_ERR_UNSUPPORTED); D 64 or 128.
  * Offsets or lengths outside the tensors (or a sequence longer than
  * max_seqlen_q) are clamped on the device and set bit 4 of the device status
  * word; the output is then unspecified.

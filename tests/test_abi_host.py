@@ -161,7 +161,7 @@ def test_varlen_rejects_bad_arguments(L):
     assert call(18, -2) == 1          # window
     assert call(12, 96) == 2          # D
     assert call(21, 1) == 2           # fp32 not built
-    assert call(21, 2) == 2           # fp16 varlen not built
+    assert call(21, 7) == 1           # no such type
     assert call(7, P(FAKE)) == 1      # out aliasing q
 
 

@@ -19,13 +19,13 @@ def _cu(lens):
 
 
 def run_varlen(dev, Hq, Hkv, D, lens_q, lens_k, used=None, causal=True, wl=None, wr=None, softcap=None, alibi=False,
-               seed=12, extra_k=0):
+               seed=12, extra_k=0, dtype=torch.bfloat16):
     import tiled_scaled_dot_gb300 as g
     cq, ck = _cu(lens_q), _cu(lens_k)
     total_q, total_k = int(cq[-1]), int(ck[-1]) + extra_k
-    q = synth.normal((max(total_q, 1), Hq, D), seed, synth.STREAM_Q, torch.bfloat16)[:total_q]
-    k = synth.normal((total_k, Hkv, D), seed, synth.STREAM_K, torch.bfloat16)
-    v = synth.normal((total_k, Hkv, D), seed, synth.STREAM_V, torch.bfloat16)
+    q = synth.normal((max(total_q, 1), Hq, D), seed, synth.STREAM_Q, dtype)[:total_q]
+    k = synth.normal((total_k, Hkv, D), seed, synth.STREAM_K, dtype)
+    v = synth.normal((total_k, Hkv, D), seed, synth.STREAM_V, dtype)
     slopes = synth.alibi_slopes(Hq) if alibi else None
     su = None if used is None else torch.tensor(used, dtype=torch.int32)
     ref, ref_lse = oracle.attn_varlen(q, k, v, cq, ck, seqused_k=su, causal=causal, window_left=wl, window_right=wr,
@@ -36,9 +36,10 @@ def run_varlen(dev, Hq, Hkv, D, lens_q, lens_k, used=None, causal=True, wl=None,
                             causal=causal, window_left=wl, window_right=wr, softcap=softcap, lse=lse)
     torch.cuda.synchronize()
     assert g.device_status() == 0
-    what = f"varlen Hq{Hq} Hkv{Hkv} D{D} q{lens_q[:5]} k{lens_k[:5]} c{causal} w({wl},{wr}) cap{softcap} alibi{alibi}"
-    check_out(out, ref, torch.bfloat16, what)
-    check_lse(lse, ref_lse, torch.bfloat16, what)
+    what = f"varlen {dtype} Hq{Hq} Hkv{Hkv} D{D} q{lens_q[:5]} k{lens_k[:5]} c{causal} w({wl},{wr}) cap{softcap} alibi{alibi}"
+    assert out.dtype == dtype
+    check_out(out, ref, dtype, what)
+    check_lse(lse, ref_lse, dtype, what)
     return out
 
 
@@ -93,3 +94,15 @@ def test_varlen_many_sequences_mixed_lengths(cuda_device):
     """A serving-like mix: 24 sequences of 1 .. 2048 queries, GQA 4."""
     lens = (1 + synth.randint(24, 2048, 3, 6)).tolist()
     run_varlen(cuda_device, 16, 4, 128, lens, lens, causal=True)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("flags", [dict(), dict(softcap=20.0, alibi=True, wl=300, wr=0)],
+                         ids=["plain", "softcap-alibi-window"])
+def test_varlen_fp16(cuda_device, D, flags):
+    """fp16 packed sequences: fp16 operands and P on the tensor cores, fp16 output
+    (attention.fkc.md lists F16 among the input types); the 16-bit bars."""
+    run_varlen(cuda_device, 8, 2, D, [1, 300, 129, 700], [1, 300, 200, 700], causal=True, dtype=torch.float16,
+               **flags)
+    lens = (1 + synth.randint(12, 1500, 4, 6)).tolist()
+    run_varlen(cuda_device, 8, 4, D, lens, lens, causal=True, dtype=torch.float16, **flags)

@@ -248,13 +248,15 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, seqused_k
                     lse=None, stream=None):
     """Packed variable-length attention (see attn_fwd_varlen in gbattn.h).
 
-    q [total_q, Hq, D], k / v [total_k, Hkv, D] bf16; cu_seqlens_q / cu_seqlens_k
+    q [total_q, Hq, D], k / v [total_k, Hkv, D] bf16 or fp16; cu_seqlens_q / cu_seqlens_k
     int32 [B + 1] and seqused_k int32 [B] (optional), all CUDA; max_seqlen_q an
     int at least every sequence's query count.  Causal masks align bottom-right.
     lse (optional) fp32 [Hq, total_q].  Returns out [total_q, Hq, D].
     """
+    if q.dtype not in _DT16:
+        raise TypeError(f"packed sequences take bf16 or fp16, got {q.dtype}")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, torch.bfloat16, 3)
+        _check(t, n, q.dtype, 3)
     for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k"), (seqused_k, "seqused_k")):
         if t is not None:
             _check(t, n, torch.int32, 1)
@@ -270,14 +272,14 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, seqused_k
     if out is None:
         out = torch.empty_like(q)
     else:
-        _check(out, "out", torch.bfloat16, 3)
+        _check(out, "out", q.dtype, 3)
     if lse is not None:
         _check(lse, "lse", torch.float32)
     scale = (1.0 / math.sqrt(D)) if softmax_scale is None else float(softmax_scale)
     st = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), _ptr(seqused_k),
                                _ptr(alibi_slopes), _ptr(out), _ptr(lse), B, Hq, Hkv, D, total_q, total_k,
                                int(max_seqlen_q), scale, 1 if causal else 0, _win(window_left), _win(window_right),
-                               float(softcap or 0.0), GBATTN_BF16, _stream_handle(stream))
+                               float(softcap or 0.0), _DT16[q.dtype], _stream_handle(stream))
     if st:
         raise GbattnError(st, "attn_fwd_varlen")
     return out

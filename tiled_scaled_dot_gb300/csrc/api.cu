@@ -260,7 +260,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* 
     if (rc) return rc;
     if ((long long)total_q * Hq > 0x7fffffffLL || (long long)total_k * Hkv > 0x7fffffffLL)
         return GBATTN_ERR_UNSUPPORTED;
-    if (dtype != GBATTN_BF16) return GBATTN_ERR_UNSUPPORTED;
+    if (dtype == GBATTN_F32) return GBATTN_ERR_UNSUPPORTED;
     if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return GBATTN_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return GBATTN_ERR_INVALID_ARG;
     if (window_left < -1 || window_right < -1) return GBATTN_ERR_INVALID_ARG;
@@ -294,6 +294,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* 
     f.softcap = softcap;
     f.timeout_ns = g_timeout_ns;
     f.varlen = 1;
+    f.f16 = dtype == GBATTN_F16;
     f.cu_q = cu_seqlens_q;
     f.cu_k = cu_seqlens_k;
     f.used_k = seqused_k;
@@ -301,8 +302,9 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, const int32_t* 
     f.total_k = total_k;
     if (!device_facts(&f.status, &f.num_sms)) return GBATTN_ERR_CUDA;
     CUtensorMap tq, tk, tv, to;
-    if (!cached_map(&tq, q, D, Hq, total_q, 128, 1) || !cached_map(&tk, k, D, Hkv, total_k, 128, 1) ||
-        !cached_map(&tv, v, D, Hkv, total_k, 128, 1) || !cached_map(&to, out, D, Hq, total_q, 128, 1))
+    const bool h = f.f16 != 0;
+    if (!cached_map(&tq, q, D, Hq, total_q, 128, 1, h) || !cached_map(&tk, k, D, Hkv, total_k, 128, 1, h) ||
+        !cached_map(&tv, v, D, Hkv, total_k, 128, 1, h) || !cached_map(&to, out, D, Hq, total_q, 128, 1, h))
         return GBATTN_ERR_CUDA;
     cudaError_t e = launch_prefill_bf16(f, tq, tk, tv, to, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;

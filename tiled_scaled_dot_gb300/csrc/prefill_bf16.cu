@@ -962,8 +962,9 @@ cudaError_t launch_prefill_bf16(const FwdProblem& f, const CUtensorMap& tq, cons
     p.n_items = (int)n_items;
     const int grid = p.n_items < f.num_sms ? p.n_items : f.num_sms;
     const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
-    // packed sequences are built for bf16 only
-    if (p.varlen) return launch_flags<true, false>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream);
+    if (p.varlen)
+        return f.f16 ? launch_flags<true, true>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream)
+                     : launch_flags<true, false>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream);
     return f.f16 ? launch_flags<false, true>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream)
                  : launch_flags<false, false>(p, grid, f.D, cap, ali, tq, tk, tv, to, stream);
 }
