@@ -366,9 +366,49 @@ def e2e_prefill(g, w, base, args, ws, stream, flops):
     run(max(2, args.warmup))
     ms = max_over_ranks(run(args.steps), ws)
     tf = flops / (ms / args.steps * 1e-3) / 1e12 * ws
+    per = ms / args.steps
+    link = host_link_bandwidth(h2d, d2h, args.steps)
     return {"value": round(tf, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / args.steps, 4),
-            "pipelining": "upload of step i + 1 and download of step i - 1 overlap step i (two buffer sets)"}
+            "ms_per_step": round(per, 4),
+            "pipelining": "upload of step i + 1 and download of step i - 1 overlap step i (two buffer sets)",
+            "link": dict(link, frac=round(link["concurrent_ms"] / per, 4))}
+
+
+def host_link_bandwidth(h2d, d2h, reps):
+    """The host link's own ceiling for one step's copies: pinned-memory copies
+    of the same byte counts (h2d up on one stream while d2h comes down on
+    another), timed with CUDA events, with no kernel between them.  `frac` in
+    the e2e object is this time over the measured step time."""
+    up_h = torch.empty(h2d, dtype=torch.uint8, pin_memory=True)
+    dn_h = torch.empty(d2h, dtype=torch.uint8, pin_memory=True)
+    up_d = torch.empty(h2d, dtype=torch.uint8, device="cuda")
+    dn_d = torch.empty(d2h, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(up, down):
+        torch.cuda.synchronize()
+        e0, e1, mid = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                       torch.cuda.Event())
+        e0.record(s1)
+        s2.wait_event(e0)
+        for _ in range(reps):
+            if up:
+                with torch.cuda.stream(s1):
+                    up_d.copy_(up_h, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s2):
+                    dn_h.copy_(dn_d, non_blocking=True)
+        mid.record(s2)
+        s1.wait_event(mid)
+        e1.record(s1)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    timed(True, True)
+    t_up, t_dn, t_both = timed(True, False), timed(False, True), timed(True, True)
+    return {"h2d_gbs": round(h2d / (t_up * 1e-3) / 1e9, 1), "d2h_gbs": round(d2h / (t_dn * 1e-3) / 1e9, 1),
+            "concurrent_ms": round(t_both, 4),
+            "what": "pinned-memory copies of one step's bytes, up and down at once, no kernel"}
 
 
 def bench_decode(g, args, ws, dev, pk):
