@@ -187,14 +187,14 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch, one-pass ncu
     # captures of the full-size workloads (values as ncu prints them)
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "869b8c2e02d5fd44"): 130418176,
-    ("prefill", "bf16_causal_b1_h32_s8192_d128", "869b8c2e02d5fd44"): 134603776,
-    ("prefill", "bf16_masked_b2_h16_s4096_d64", "869b8c2e02d5fd44"): 51266560,
-    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "869b8c2e02d5fd44"): 1778597888,
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "20cc43071f094d9e"): 2155364096,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "20cc43071f094d9e"): 1749039616,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "889136898a718355"): 341057536,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "889136898a718355"): 215400960,
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "7b0c74527ec283dc"): 130112000,
+    ("prefill", "bf16_causal_b1_h32_s8192_d128", "7b0c74527ec283dc"): 134455552,
+    ("prefill", "bf16_masked_b2_h16_s4096_d64", "7b0c74527ec283dc"): 51258368,
+    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "7b0c74527ec283dc"): 1778246144,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "9bb92366914cbb73"): 2155266304,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "9bb92366914cbb73"): 1749257216,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "c91522c47886322d"): 340972800,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "c91522c47886322d"): 215552768,
 }
 
 
