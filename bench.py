@@ -181,7 +181,7 @@ def max_over_ranks(x: float, ws: int) -> float:
 KERNEL_SOURCES = {
     # api.cu chooses the tensor-map boxes, grids and split plans of every launch
     "prefill": ("prefill_bf16.cu", "ptx.cuh", "kernels.h", "api.cu"),
-    "decode": ("decode_bf16.cu", "ptx.cuh", "kernels.h", "api.cu"),
+    "decode": ("decode_bf16.cu", "decode_balanced.cu", "decode_common.cuh", "ptx.cuh", "kernels.h", "api.cu"),
     "backward": ("backward_bf16.cu", "ptx.cuh", "kernels.h", "api.cu"),
 }
 NCU_TRAFFIC = {

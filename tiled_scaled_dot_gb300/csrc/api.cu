@@ -566,6 +566,7 @@ int attn_decode(const void* q, const void* k, const void* v, const float* alibi_
     f.scale = softmax_scale;
     f.softcap = softcap;
     f.wl = window_left;
+    f.auto_splits = num_splits == 0;
     f.timeout_ns = g_timeout_ns;
     f.f16 = dtype == GBATTN_F16;
     CUtensorMap tk, tv;
@@ -642,6 +643,7 @@ int attn_decode_paged(const void* q, const void* k_cache, const void* v_cache, c
     f.scale = softmax_scale;
     f.softcap = softcap;
     f.wl = window_left;
+    f.auto_splits = num_splits == 0;
     f.timeout_ns = g_timeout_ns;
     f.paged = 1;
     f.block_table = block_table;

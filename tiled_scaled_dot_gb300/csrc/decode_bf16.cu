@@ -1,14 +1,11 @@
-// decode_bf16.cu -- split-KV decode (one query row per head) and the
-// log-sum-exp combine of the partial results.
-//
-// "gfx942 unified attention, from the math up", section 8: with one query
-// row, parallelism comes from splitting the keys across thread blocks and
-// combining the partial softmax-weighted outputs.  The combine is the online
-// recurrence of section 3 applied across splits: LSE = log sum_s e^{lse_s},
-// O = sum_s e^{lse_s - LSE} O_s, evaluated in a fixed split order.
+// decode_bf16.cu -- split-KV decode (one query row per head), the split
+// plan, and the launches of the decode kernels and of the log-sum-exp combine.
 //
 // The path is bound by HBM reads of K and V, so it runs on the SIMT pipes:
-//   * one CTA per (batch, kv head, head chunk, split); all query heads of a
+//   * one CTA per (batch, kv head, head chunk, split) in this file's kernel
+//     (fixed splits: an explicit split count, or a plan of one split); the
+//     balanced kernel (decode_balanced.cu) serves automatic multi-split plans
+//     with equal shares of all streams' tiles per CTA; all query heads of a
 //     GQA group (up to GC of them) are served from one read of each key;
 //   * a producer warp streams 64-key K and V tiles with TMA into a 3-stage
 //     shared-memory ring (128-byte swizzle, so the consumers' row reads are
@@ -23,73 +20,12 @@
 // Template flags: PAGED reads K and V through a block table from a pool
 // [num_blocks, block_size, Hkv, D] (attention.fkc.md, "attention_paged_naive"),
 // with per-sequence context lengths; F16 reads and writes fp16 instead of bf16.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "kernels.h"
-#include "ptx.cuh"
+#include "decode_common.cuh"
 
 namespace gbattn {
 namespace {
 
-constexpr int TILE = 64;     // keys per tile
-constexpr int NSTG = 3;      // ring stages
-constexpr int CONSUMERS = 4; // consumer warps
-constexpr int DEC_THREADS = (CONSUMERS + 1) * 32;
-constexpr float LOG2E = 1.4426950408889634f;
-constexpr float LN2 = 0.6931471805599453f;
-
-struct DecParams {
-    const uint16_t* q;   // bf16 or fp16 bits
-    uint16_t* out;
-    float* lse;
-    const float* slopes;
-    float* ws_o;
-    float* ws_lse;
-    unsigned int* status;
-    unsigned long long timeout_ns;
-    int B, Hq, Hkv, Sk, G;
-    int n_chunks;       // head chunks per kv head
-    int num_splits;
-    int chunk_tiles;    // tiles per split
-    int n_tiles;        // tiles over Sk
-    float qscale;       // multiplies q: scale * log2(e) (no softcap) or scale (softcap)
-    float softcap;
-    int wl;             // left window (-1: none): keys j >= len - 1 - wl
-    // paged cache: tile t of sequence b gathers keys [64 t, 64 t + 64) block by block
-    const uint32_t* block_table;   // [B, max_blocks]
-    const uint32_t* context_lens;  // [B]
-    int max_blocks, bs_log2, num_blocks;
-};
-
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-// low / high 16-bit element of a packed pair, bf16 or fp16
-template <bool F16>
-__device__ __forceinline__ float lo16(uint32_t w) {
-    return F16 ? __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))) : bf16lo(w);
-}
-template <bool F16>
-__device__ __forceinline__ float hi16(uint32_t w) {
-    return F16 ? __half2float(__ushort_as_half((unsigned short)(w >> 16))) : bf16hi(w);
-}
-// fp32 -> the 16-bit storage type (round to nearest even), as bits
-template <bool F16>
-__device__ __forceinline__ uint16_t to16(float v) {
-    return F16 ? __half_as_ushort(__float2half_rn(v)) : __bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-
-template <int D>
-struct DCfg {
-    static constexpr int SLABS = D / 64;
-    static constexpr int SLAB = TILE * 128;           // bytes of one 64-wide slab of a tile
-    static constexpr int TILE_BYTES = TILE * D * 2;   // K or V tile
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-    static constexpr int SMEM = NSTG * STAGE_BYTES + 1024;
-};
-
-// Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled slab.
-__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+using namespace dec;
 
 template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED, bool F16>
 __global__ void __launch_bounds__(DEC_THREADS, 2)
@@ -409,29 +345,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     }
 }
 
-// Combine: one block per (b, h) row, one thread per output dimension.
-template <int D, bool F16>
-__global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restrict__ ws_o,
-                                                           const float* __restrict__ ws_lse,
-                                                           uint16_t* __restrict__ out, float* __restrict__ lse,
-                                                           int num_splits, float lse_to_natural) {
-    const size_t row = blockIdx.x;
-    const int d = threadIdx.x;
-    const float* ls = ws_lse + row * num_splits;
-    float M = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) M = fmaxf(M, ls[s]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < num_splits; ++s) {
-            const float w = (ls[s] == -INFINITY) ? 0.f : ex2_approx(ls[s] - M);
-            L += w;
-            O += w * ws_o[(row * num_splits + s) * D + d];
-        }
-    }
-    out[row * D + d] = to16<F16>(L > 0.f ? O / L : 0.f);
-    if (lse && d == 0) lse[row] = (L > 0.f) ? (M + log2f(L)) * lse_to_natural : -INFINITY;
-}
-
 template <int D, int GC, bool SOFTCAP, bool ALIBI, bool PAGED, bool F16>
 cudaError_t launch_dec(const DecParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
     auto kern = decode_bf16_kernel<D, GC, SOFTCAP, ALIBI, PAGED, F16>;
@@ -440,10 +353,6 @@ cudaError_t launch_dec(const DecParams& p, const CUtensorMap& tk, const CUtensor
     if (e != cudaSuccess) return e;
     const long long grid = (long long)p.B * p.Hkv * p.n_chunks * p.num_splits;
     kern<<<(unsigned)grid, DEC_THREADS, smem, stream>>>(tk, tv, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || p.num_splits == 1) return e;
-    // every partial lse is in base 2 (logits carry the log2(e) factor).
-    decode_combine_kernel<D, F16><<<p.B * p.Hq, D, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits, LN2);
     return cudaGetLastError();
 }
 
@@ -538,19 +447,53 @@ cudaError_t launch_decode_bf16(const DecodeProblem& f, const CUtensorMap& tk, co
     const bool cap = f.softcap > 0.f, ali = f.slopes != nullptr;
     p.qscale = cap ? f.scale : f.scale * LOG2E;
     const int G = p.G;
-    if (f.D == 128) {
-        const int GC = G >= 4 ? 4 : (G == 3 ? 4 : (G == 2 ? 2 : 1));
-        p.n_chunks = (G + GC - 1) / GC;
-        if (GC == 4) return launch_dec_flags<128, 4>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
-        if (GC == 2) return launch_dec_flags<128, 2>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
-        return launch_dec_flags<128, 1>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
-    }
-    const int GC = G >= 5 ? 8 : (G >= 3 ? 4 : (G == 2 ? 2 : 1));
+    const int GC = f.D == 128 ? (G >= 3 ? 4 : (G == 2 ? 2 : 1)) : (G >= 5 ? 8 : (G >= 3 ? 4 : (G == 2 ? 2 : 1)));
     p.n_chunks = (G + GC - 1) / GC;
-    if (GC == 8) return launch_dec_flags<64, 8>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
-    if (GC == 4) return launch_dec_flags<64, 4>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
-    if (GC == 2) return launch_dec_flags<64, 2>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
-    return launch_dec_flags<64, 1>(p, cap, ali, paged, f.f16 != 0, tk, tv, stream);
+    const bool f16 = f.f16 != 0;
+    cudaError_t e;
+    // An automatic multi-split plan runs balanced when the fixed splits would
+    // leave SMs idle at the end: the CTAs (two per SM) take equal shares of all
+    // streams' tiles laid end to end.  That pays for uneven paged contexts and
+    // for fixed-split grids of under four waves (a partial last wave weighs a
+    // quarter or more); with more waves the fixed-split kernel is as fast (on
+    // GB300: B64 Hkv8 Sk8192, 6.7 waves: 6450 GB/s fixed against 6296 balanced;
+    // B16, 3.4 waves: 5162 against 5422; paged with contexts 4096..8192: 5819
+    // against 6018).
+    const int slots = 2 * (f.num_sms > 0 ? f.num_sms : 1);
+    const long long fixed_ctas = (long long)f.B * f.Hkv * p.n_chunks * f.num_splits;
+    if (f.auto_splits && f.num_splits >= 2 && (paged || fixed_ctas < 4LL * slots)) {
+        p.grid_balanced = slots;
+        e = launch_balanced(p, f.D, GC, cap, ali, paged, f16, tk, tv, stream);
+    } else if (f.D == 128) {
+        e = GC == 4   ? launch_dec_flags<128, 4>(p, cap, ali, paged, f16, tk, tv, stream)
+            : GC == 2 ? launch_dec_flags<128, 2>(p, cap, ali, paged, f16, tk, tv, stream)
+                      : launch_dec_flags<128, 1>(p, cap, ali, paged, f16, tk, tv, stream);
+    } else {
+        e = GC == 8   ? launch_dec_flags<64, 8>(p, cap, ali, paged, f16, tk, tv, stream)
+            : GC == 4 ? launch_dec_flags<64, 4>(p, cap, ali, paged, f16, tk, tv, stream)
+            : GC == 2 ? launch_dec_flags<64, 2>(p, cap, ali, paged, f16, tk, tv, stream)
+                      : launch_dec_flags<64, 1>(p, cap, ali, paged, f16, tk, tv, stream);
+    }
+    if (e != cudaSuccess || p.num_splits == 1) return e;
+    // every partial lse is in base 2 (logits carry the log2(e) factor)
+    const uint32_t* lens = paged ? p.context_lens : nullptr;
+    const unsigned rows = (unsigned)(p.B * p.Hq);
+    if (f.D == 128) {
+        if (f16)
+            decode_combine_kernel<128, true><<<rows, 128, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
+                                                                       LN2, lens, p.Hq);
+        else
+            decode_combine_kernel<128, false><<<rows, 128, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
+                                                                        LN2, lens, p.Hq);
+    } else {
+        if (f16)
+            decode_combine_kernel<64, true><<<rows, 64, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
+                                                                     LN2, lens, p.Hq);
+        else
+            decode_combine_kernel<64, false><<<rows, 64, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
+                                                                      LN2, lens, p.Hq);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace gbattn

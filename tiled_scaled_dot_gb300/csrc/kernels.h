@@ -47,6 +47,7 @@ struct DecodeProblem {
     float softcap;
     int wl;                     // left window at the query's position (the last key); -1 = none
     int num_splits;             // resolved (>= 1)
+    int auto_splits;            // num_splits came from the automatic plan (the caller asked for 0)
     int chunk;                  // keys per split, multiple of 64
     float* ws_o;                // [B, Hq, num_splits, D] fp32 (num_splits > 1)
     float* ws_lse;              // [B, Hq, num_splits] fp32 (num_splits > 1)
