@@ -187,14 +187,14 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch, one-pass ncu
     # captures of the full-size workloads (values as ncu prints them)
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "7b0c74527ec283dc"): 130112000,
-    ("prefill", "bf16_causal_b1_h32_s8192_d128", "7b0c74527ec283dc"): 134455552,
-    ("prefill", "bf16_masked_b2_h16_s4096_d64", "7b0c74527ec283dc"): 51258368,
-    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "7b0c74527ec283dc"): 1778246144,
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "9bb92366914cbb73"): 2155266304,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "9bb92366914cbb73"): 1749257216,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "c91522c47886322d"): 340972800,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "c91522c47886322d"): 215552768,
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "63ac4a96265bae59"): 130319360,
+    ("prefill", "bf16_causal_b1_h32_s8192_d128", "63ac4a96265bae59"): 133592064,
+    ("prefill", "bf16_masked_b2_h16_s4096_d64", "63ac4a96265bae59"): 51061504,
+    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "63ac4a96265bae59"): 1789548544,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "809a4f93da2a3b07"): 2154978304,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "809a4f93da2a3b07"): 1747040512,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "418e97a5dca29fde"): 338917376,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "418e97a5dca29fde"): 216192256,
 }
 
 
