@@ -332,7 +332,9 @@ int attn_bwd(const gbattn_bwd_params* p);
  * (1 .. 100000) with CUDA events recorded on p->stream between its launches,
  * waits for each run, and writes the mean milliseconds of its four phases to
  * phase_ms[4]: the forward recompute (0 when out and lse are given), the prep
- * launches (row intervals, Delta), the dK / dV launch and the dQ launch.  The
+ * launches (row intervals; for fp32 also Delta = dO . O), the dK / dV launch and
+ * the dQ launch.  For bf16 / fp16 the dQ launch runs before the dK / dV launch
+ * and also forms Delta and the base-2 lse.  The
  * gradients are written as by attn_bwd.  Synchronous; creates and destroys its
  * own events.
  */

@@ -448,13 +448,14 @@ static int bwd_run(const gbattn_bwd_params* a, cudaEvent_t* ev) {
         return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
     }
     const bool h = b.f16 != 0;
-    CUtensorMap tq, tdo, tk, tv;
+    CUtensorMap tq, tdo, tk, tv, to;
     if (!cached_map(&tq, a->q, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h) ||
         !cached_map(&tdo, a->dout, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h) ||
         !cached_map(&tk, a->k, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h) ||
-        !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h))
+        !cached_map(&tv, a->v, a->D, a->Sk, (uint64_t)a->B * a->Hkv, 128, 0, h) ||
+        !cached_map(&to, out, a->D, a->Sq, (uint64_t)a->B * a->Hq, 128, 0, h))
         return GBATTN_ERR_CUDA;
-    cudaError_t e = launch_backward_bf16(b, tq, tdo, tk, tv, static_cast<cudaStream_t>(a->stream),
+    cudaError_t e = launch_backward_bf16(b, tq, tdo, tk, tv, to, static_cast<cudaStream_t>(a->stream),
                                          ev ? ev + 1 : nullptr);
     return e == cudaSuccess ? GBATTN_OK : GBATTN_ERR_CUDA;
 }
@@ -481,8 +482,14 @@ int attn_bwd_phase_times(const gbattn_bwd_params* a, int reps, float* phase_ms) 
         }
     }
     for (int i = 0; i < 5; ++i) cudaEventDestroy(ev[i]);
-    if (rc == GBATTN_OK)
+    if (rc == GBATTN_OK) {
         for (int i = 0; i < 4; ++i) phase_ms[i] = (float)(acc[i] / reps);
+        if (a->dtype != GBATTN_F32) {
+            // the 16-bit path launches dQ before dK / dV
+            phase_ms[2] = (float)(acc[3] / reps);
+            phase_ms[3] = (float)(acc[2] / reps);
+        }
+    }
     return rc;
 }
 

@@ -10,20 +10,22 @@
 // where Delta_i = sum_j P_ij dP_ij = dO_i . O_i (O the forward output), and
 // dK / dV of a kv head sum over the query heads of its GQA group.
 //
-// Four launches, all deterministic (no atomics, fixed summation order):
+// Three launches, all deterministic (no atomics, fixed summation order):
 //   bwd_rows_kernel    per query row its admissible key interval [a, e]
 //                      (causal, window, row bounds, Sk) and per 128-row query
 //                      tile a summary: the span of its live rows' intervals
 //                      and the tightest interval common to all its rows;
-//   bwd_delta_kernel   per (b, h, row) Delta = dO . O and the base-2 lse
-//                      (+inf for a row with no admissible key, so P = 0);
+//   bwd_kernel<DQ=1>   one work item per (b, head, 128-row query tile): S =
+//                      Q K^T, dP = dO V^T for every admissible key tile,
+//                      dQ += dS K accumulated in TMEM.  The item's O tile
+//                      comes through the streamed-tile ring ahead of its first
+//                      K tile; each row's Delta = dO . O is formed from it and
+//                      written with the row's base-2 lse (+inf for a row with
+//                      no admissible key, so P = 0) for the next launch;
 //   bwd_kernel<DQ=0>   one work item per (b, kv head, 128-key tile): S^T =
 //                      K Q^T and dP^T = V dO^T for every admissible 128-row
 //                      query tile of every head of the group, dV += P^T dO
-//                      and dK += dS^T Q accumulated in TMEM;
-//   bwd_kernel<DQ=1>   one work item per (b, head, 128-row query tile): S =
-//                      Q K^T, dP = dO V^T for every admissible key tile,
-//                      dQ += dS K accumulated in TMEM.
+//                      and dK += dS^T Q accumulated in TMEM.
 // The two main launches are one template: a pair of "fixed" tiles per item
 // (K, V or Q, dO) stays in shared memory while pairs of "streamed" tiles
 // (Q, dO or K, V) move one tile at a time through a ring of NSLOT shared-memory
@@ -89,7 +91,7 @@ struct BCfg {
     // beside the fixed tiles in 227 KB
     static constexpr int NSLOT = DQ ? (D == 128 ? 5 : 10) : (D == 128 ? 4 : 8);
     static constexpr int SMEM_BYTES = 2 * TILE_BYTES + NSLOT * TILE_BYTES + (DQ ? 0 : NSLOT * EXTRA_BYTES) + 1024;
-    static_assert(NSLOT <= MAX_SLOTS && SMEM_BYTES <= 232448 - 512, "shared memory");
+    static_assert(NSLOT <= MAX_SLOTS && SMEM_BYTES <= 232448 - 1536, "shared memory");
     static constexpr uint32_t ACC1 = 256;      // dV (DQ = 0) or dQ (DQ = 1)
     static constexpr uint32_t ACC2 = 256 + D;  // dK (DQ = 0)
 };
@@ -100,6 +102,9 @@ struct BParams {
     uint16_t* dv;  // [B, Hkv, Sk, D]
     const float* lse2;   // [B * Hq][Sq_pad] base-2 lse (+inf: no admissible key, or padding)
     const float* delta;  // [B * Hq][Sq_pad]
+    float* lse2_w;       // the same arrays, written by the DQ = 1 launch
+    float* delta_w;
+    const float* lse;    // [B, Hq, Sq] natural-log lse of the forward
     const int2* rows;    // [B][Sq_pad] admissible key interval of each query row
     const int4* summ;    // [B][n_qt] per query tile: (lo_live, hi_live, a_max, e_min)
     const float* slopes;
@@ -191,51 +196,6 @@ __global__ void __launch_bounds__(TR) bwd_rows_kernel(const int2* __restrict__ r
     }
 }
 
-// ---------------------------------------------------------------------------- Delta and base-2 lse
-// Per padded row (b h, i): Delta = dO . O in fp32, lse2 = lse * log2(e).  A
-// row is D / 8 lanes with one 16-byte load of dO and of O each, so a warp
-// takes 32 / (D / 8) rows per pass.
-template <int D, bool F16>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ dout,
-                                                        const uint16_t* __restrict__ out,
-                                                        const float* __restrict__ lse, float* __restrict__ lse2,
-                                                        float* __restrict__ delta, long long n_rows, int Sq,
-                                                        int Sq_pad) {
-    constexpr int LPR = D / 8;     // lanes per row
-    constexpr int RPW = 32 / LPR;  // rows per warp and pass
-    const int lane = threadIdx.x & 31, sub = lane / LPR, l = lane % LPR;
-    const long long w0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    for (long long base = w0 * RPW; base < n_rows; base += nw * RPW) {
-        const long long row = base + sub;
-        float d = 0.f, l2 = INFINITY;
-        if (row < n_rows) {
-            const long long bh = row / Sq_pad;
-            const int i = (int)(row - bh * Sq_pad);
-            if (i < Sq) {
-                const size_t off = ((size_t)bh * Sq + i) * D + l * 8;
-                const uint4 a = *reinterpret_cast<const uint4*>(dout + off);
-                const uint4 c = *reinterpret_cast<const uint4*>(out + off);
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    d = fmaf(widen16<F16>((uint16_t)(aw[t] & 0xffffu)), widen16<F16>((uint16_t)(cw[t] & 0xffffu)), d);
-                    d = fmaf(widen16<F16>((uint16_t)(aw[t] >> 16)), widen16<F16>((uint16_t)(cw[t] >> 16)), d);
-                }
-                const float lv = lse[(size_t)bh * Sq + i];
-                l2 = (lv == -INFINITY) ? INFINITY : lv * LOG2E;
-            }
-        }
-        // sum over the row's lanes (every lane takes part)
-#pragma unroll
-        for (int o = LPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        if (row < n_rows && l == 0) {
-            lse2[row] = l2;
-            delta[row] = d;
-        }
-    }
-}
-
 // ---------------------------------------------------------------------------- work items
 // DQ = 0: item -> (b, kv head, key tile n), lowest n first (under a top-left
 // causal mask the first key tiles meet the most query tiles).
@@ -290,8 +250,10 @@ struct BSmem {
     uint64_t s_full, dp_full, s_free, acc_full, acc_empty;
     uint64_t p_half[2], ds_half[2];  // P / dS of columns 64 g + 32 h .. + 31 of both groups are in TMEM
     uint64_t drain;
+    uint64_t delta_bar;  // DQ = 1: both column groups' Delta halves are written
     uint32_t tmem_base;
     int abort_flag;
+    float dpart[2][TR];  // DQ = 1: Delta halves per column group and row
 };
 
 // The steps of an item, enumerated the same way by every role.
@@ -356,13 +318,39 @@ __device__ __forceinline__ void store_row32(uint16_t* dst, const float (&v)[32],
     }
 }
 
+// This column group's half of dO_i . O_i in fp32: D / 2 dimensions of row r
+// of two 128 x D tiles in shared memory (64-column slabs, 128-byte swizzle);
+// group g takes slab g (D = 128) or chunks 4 g .. 4 g + 3 of the one slab
+// (D = 64).  Two accumulators over even and odd dimensions, fixed order.
+template <int D, bool F16>
+__device__ __forceinline__ float half_row_dot(const uint8_t* a, const uint8_t* o, int g, int r) {
+    constexpr int CH = D / 16;
+    const int slab = D == 128 ? g : 0, cb = D == 128 ? 0 : 4 * g;
+    const uint8_t* pa = a + slab * (TR * 128) + r * 128;
+    const uint8_t* po = o + slab * (TR * 128) + r * 128;
+    float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int off = ((cb + c) ^ (r & 7)) << 4;
+        const uint4 x = *reinterpret_cast<const uint4*>(pa + off);
+        const uint4 y = *reinterpret_cast<const uint4*>(po + off);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            d0 = fmaf(widen16<F16>((uint16_t)(xw[t] & 0xffffu)), widen16<F16>((uint16_t)(yw[t] & 0xffffu)), d0);
+            d1 = fmaf(widen16<F16>((uint16_t)(xw[t] >> 16)), widen16<F16>((uint16_t)(yw[t] >> 16)), d1);
+        }
+    }
+    return d0 + d1;
+}
+
 __device__ __forceinline__ void zero_row(uint16_t* dst, int n) {
     for (int i = 0; i < n / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
 }
 
 template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
 __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tmem, const WaitCtl& wc, int warp,
-                                        const uint8_t* sX) {
+                                        const uint8_t* sX, const uint8_t* sF2, const uint8_t* sT) {
     using C = BCfg<D, DQ>;
     const int g = warp >> 2;          // column group: columns 64 g .. 64 g + 63
     const int r = threadIdx.x & (TR - 1);  // TMEM lane
@@ -372,6 +360,7 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
     const uint32_t tDP = tmem + lane_off + 128 + c0;  // dP; packed dS at its first 32 columns
     const int grid = gridDim.x, cta = blockIdx.x;
     uint32_t step = 0, acc_cnt = 0, stg = 0;
+    uint32_t nlive = 0, dcnt = 0;  // items with steps so far; Delta exchanges so far (DQ = 1)
     for (int k = 0;; ++k) {
         const int item = item_of(k, cta, grid);
         if (item >= p.n_items) break;
@@ -382,6 +371,11 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
             if (DQ) {
                 const int i = it.t * TR + r;
                 if (i < p.Sq) zero_row(p.dq + ((size_t)(it.b * p.Hq + it.hd) * p.Sq + i) * D + g * (D / 2), D / 2);
+                if (g == 0) {
+                    const size_t prow = (size_t)(it.b * p.Hq + it.hd) * p.Sq_pad + i;
+                    p.lse2_w[prow] = INFINITY;
+                    p.delta_w[prow] = 0.f;
+                }
             } else {
                 const int key = it.t * TR + r;
                 if (key < p.Sk) zero_row((g ? p.dk : p.dv) + ((size_t)(it.b * p.Hkv + it.hd) * p.Sk + key) * D, D);
@@ -396,9 +390,17 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
             const int2 iv = __ldg(p.rows + (size_t)it.b * p.Sq_pad + i);
             ra = iv.x;
             rb = iv.y;
-            lse2_i = __ldg(p.lse2 + (size_t)(it.b * p.Hq + it.hd) * p.Sq_pad + i);
-            delta_i = __ldg(p.delta + (size_t)(it.b * p.Hq + it.hd) * p.Sq_pad + i);
+            if (i < p.Sq) {
+                const float lv = __ldg(p.lse + (size_t)(it.b * p.Hq + it.hd) * p.Sq + i);
+                lse2_i = (lv == -INFINITY) ? INFINITY : lv * LOG2E;
+            }
         }
+        // DQ = 1: fill index of the item's O tile (the producer loads it into the
+        // ring ahead of the item's first K tile), and the item's fixed-tile phase
+        const uint32_t f_o = 2 * stg + nlive;
+        const uint32_t fix_par = nlive & 1u;
+        ++nlive;
+        bool first = true;
         const bool ok = for_steps<DQ>(p, it, [&](int h, int u) -> bool {
             const uint32_t f1 = 2 * stg;  // fill index of the step's T1 tile (its extras sit beside it)
             const int st = (int)(f1 % C::NSLOT);
@@ -517,6 +519,29 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
                 else
                     p_loop(std::false_type{});
             }
+            if (DQ && first) {
+                // Delta_i = dO_i . O_i: each column group takes half of the
+                // dimensions from the fixed dO tile and the item's O tile, and
+                // the halves meet in shared memory.  The exchange buffer is
+                // rewritten one item later, after every thread has passed this
+                // item's first dS hand-off (which needs Delta).
+                const int so = (int)(f_o % C::NSLOT);
+                bool w2 = mbar_wait(&sm.fix_full, fix_par, wc, ST_BWD_EW);
+                w2 = w2 && mbar_wait(&sm.slot_full[so], (f_o / C::NSLOT) & 1u, wc, ST_BWD_EW);
+                sm.dpart[g][r] = w2 ? half_row_dot<D, F16>(sF2, sT + so * C::TILE_BYTES, g, r) : 0.f;
+                mbar_arrive(&sm.delta_bar);
+                w2 = w2 && mbar_wait(&sm.delta_bar, dcnt & 1u, wc, ST_BWD_EW);
+                ++dcnt;
+                if (!__all_sync(0xffffffffu, w2)) return false;
+                const int i = it.t * TR + r;
+                delta_i = i < p.Sq ? sm.dpart[0][r] + sm.dpart[1][r] : 0.f;
+                if (g == 0) {
+                    const size_t prow = (size_t)(it.b * p.Hq + it.hd) * p.Sq_pad + i;
+                    p.lse2_w[prow] = lse2_i;
+                    p.delta_w[prow] = delta_i;
+                }
+            }
+            first = false;
             w = mbar_wait(&sm.dp_full, step & 1u, wc, ST_BWD_EW);
             if (!__all_sync(0xffffffffu, w)) return false;
             tc_fence_after();
@@ -583,7 +608,8 @@ __device__ __forceinline__ void ew_role(const BParams& p, BSmem& sm, uint32_t tm
 template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const BParams p) {
+               const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+               const __grid_constant__ CUtensorMap tmO, const BParams p) {
     using C = BCfg<D, DQ>;
     extern __shared__ __align__(1024) uint8_t dyn_smem[];
     __shared__ BSmem sm;
@@ -612,6 +638,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(&sm.acc_full, 1);
         mbar_init(&sm.acc_empty, EW_THREADS);
         mbar_init(&sm.drain, 1);
+        mbar_init(&sm.delta_bar, EW_THREADS);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
@@ -627,13 +654,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int grid = gridDim.x, cta = blockIdx.x;
 
     if (warp < 8) {
-        ew_role<D, DQ, SOFTCAP, ALIBI, F16>(p, sm, tmem, wc, warp, sX);
+        ew_role<D, DQ, SOFTCAP, ALIBI, F16>(p, sm, tmem, wc, warp, sX, sF2, sT);
     } else if (warp == WARP_PRODUCER) {
         if (lane == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmDO);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
+            if (DQ) tma_prefetch_desc(&tmO);
             uint32_t fix_cnt = 0, fills = 0;  // fills: streamed tiles loaded so far (two per step)
             bool ok = true;
             for (int k = 0; ok; ++k) {
@@ -676,10 +704,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         return true;
                     });
                 };
+                if (DQ) {
+                    // the item's O tile (for Delta) ahead of its streamed tiles; the
+                    // element-wise warps read it and the MMA warp releases it
+                    const int sl = (int)(fills % C::NSLOT);
+                    if (!(ok = mbar_wait(&sm.slot_empty[sl], ((fills / C::NSLOT) & 1u) ^ 1u, wc, ST_BWD_PRODUCER)))
+                        break;
+                    mbar_arrive_expect_tx(&sm.slot_full[sl], C::TILE_BYTES);
+#pragma unroll
+                    for (int hf = 0; hf < C::HALVES; ++hf)
+                        tma_load_3d(sT + sl * C::TILE_BYTES + hf * C::SLAB, &tmO, &sm.slot_full[sl], hf * 64,
+                                    it.t * TR, it.b * p.Hq + it.hd);
+                    ++fills;
+                }
                 // The first steps' tiles go out before the fixed tiles, which wait
                 // until the previous item's MMAs are done with theirs; the ring
-                // holds them, so this never waits on this item's own MMAs.
-                const int pre = J < C::NSLOT / 2 ? J : C::NSLOT / 2;
+                // holds them (and the O tile), so this never waits on this item's
+                // own MMAs.
+                constexpr int PRE = DQ ? (C::NSLOT - 1) / 2 : C::NSLOT / 2;
+                const int pre = J < PRE ? J : PRE;
                 fill_steps(0, pre);
                 if (!ok) break;
                 ok = mbar_wait(&sm.fix_empty, (fix_cnt & 1u) ^ 1u, wc, ST_BWD_PRODUCER);
@@ -765,6 +808,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
         uint32_t fix_cnt = 0, stg = 0, step = 0, acc_cnt = 0;
         bool ok = true;
+        // fills: DQ = 1 items load their O tile first, so fix_cnt (items with
+        // steps so far, this one included) fills precede this item's steps on
+        // top of two per step
         for (int k = 0; ok; ++k) {
             const int item = item_of(k, cta, grid);
             if (item >= p.n_items) break;
@@ -773,7 +819,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (J == 0) continue;
             ok = wwait(&sm.fix_full, fix_cnt & 1u);
             ++fix_cnt;
-            const uint32_t f0 = 2 * stg;  // fills of step j: T1 = f0 + 2 j, T2 = f0 + 2 j + 1
+            const uint32_t f0 = 2 * stg + (DQ ? fix_cnt : 0u);  // step j: T1 = f0 + 2 j, T2 = f0 + 2 j + 1
             ok = ok && wfill(f0);
             if (!ok) break;
             tc_fence_after();
@@ -828,6 +874,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = wwait(&sm.ds_half[0], step & 1u);
                     if (ok && j == 0) ok = wwait(&sm.acc_empty, (acc_cnt & 1u) ^ 1u);
                     if (!ok) break;
+                    // every element-wise thread has formed Delta: the O tile is read
+                    if (j == 0) release(f0 - 1);
                     tc_fence_after();
                     mma_ts_half(C::ACC1, 128, tile_of(t1), j > 0 ? 1u : 0u, 0);  // dQ += dS K
                     if (!(ok = wwait(&sm.ds_half[1], step & 1u))) break;
@@ -867,28 +915,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 template <int D, bool DQ, bool SOFTCAP, bool ALIBI, bool F16>
 cudaError_t launch_main(const BParams& prm, int grid, const CUtensorMap& tq, const CUtensorMap& tdo,
-                        const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream) {
+                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t stream) {
     auto kern = bwd_kernel<D, DQ, SOFTCAP, ALIBI, F16>;
     const int smem = BCfg<D, DQ>::SMEM_BYTES;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tdo, tk, tv, prm);
+    kern<<<grid, NUM_THREADS, smem, stream>>>(tq, tdo, tk, tv, to, prm);
     return cudaGetLastError();
 }
 
 template <int D, bool F16>
 cudaError_t launch_flags(const BParams& prm, int grid_a, int grid_b, bool cap, bool ali, const CUtensorMap& tq,
-                         const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream,
+                         const CUtensorMap& tdo, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& to, cudaStream_t stream,
                          cudaEvent_t* ev) {
     BParams pa = prm, pb = prm;
     pa.n_items = prm.n_kt * prm.B * prm.Hkv;
     pb.n_items = prm.n_qt * prm.B * prm.Hq;
     cudaError_t e;
+    // dQ first: it writes the Delta and base-2 lse that dK / dV reads
 #define GBATTN_BWD_PAIR(CAP, ALI)                                                              \
-    e = launch_main<D, false, CAP, ALI, F16>(pa, grid_a, tq, tdo, tk, tv, stream);              \
+    e = launch_main<D, true, CAP, ALI, F16>(pb, grid_b, tq, tdo, tk, tv, to, stream);           \
     if (e != cudaSuccess) return e;                                                             \
     if (ev && (e = cudaEventRecord(ev[2], stream)) != cudaSuccess) return e;                    \
-    e = launch_main<D, true, CAP, ALI, F16>(pb, grid_b, tq, tdo, tk, tv, stream);               \
+    e = launch_main<D, false, CAP, ALI, F16>(pa, grid_a, tq, tdo, tk, tv, to, stream);          \
     if (e != cudaSuccess) return e;                                                             \
     return ev ? cudaEventRecord(ev[3], stream) : cudaSuccess;
     if (cap) {
@@ -921,13 +971,17 @@ cudaError_t launch_backward_rows(const BwdProblem& b, cudaStream_t stream) {
 }
 
 cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, const CUtensorMap& tdo,
-                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream, cudaEvent_t* ev) {
+                                 const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                                 cudaStream_t stream, cudaEvent_t* ev) {
     BParams p{};
     p.dq = static_cast<uint16_t*>(b.dq);
     p.dk = static_cast<uint16_t*>(b.dk);
     p.dv = static_cast<uint16_t*>(b.dv);
     p.lse2 = b.ws_lse2;
     p.delta = b.ws_delta;
+    p.lse2_w = b.ws_lse2;
+    p.delta_w = b.ws_delta;
+    p.lse = b.lse;
     p.rows = reinterpret_cast<const int2*>(b.ws_rows);
     p.summ = reinterpret_cast<const int4*>(b.ws_summ);
     p.slopes = b.slopes;
@@ -953,30 +1007,6 @@ cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, con
     cudaError_t e;
     if (ev && (e = cudaEventRecord(ev[0], stream)) != cudaSuccess) return e;
     if ((e = launch_backward_rows(b, stream)) != cudaSuccess) return e;
-    // Delta and base-2 lse
-    const long long n_rows = (long long)b.B * b.Hq * p.Sq_pad;
-    long long blocks = (n_rows * 32 + 255) / 256;
-    const long long cap_blocks = (long long)b.num_sms * 16;
-    if (blocks > cap_blocks) blocks = cap_blocks;
-    const uint16_t* dO = static_cast<const uint16_t*>(b.dout);
-    const uint16_t* O = static_cast<const uint16_t*>(b.out);
-    if (b.D == 128) {
-        if (b.f16)
-            bwd_delta_kernel<128, true><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
-                                                                         b.Sq, p.Sq_pad);
-        else
-            bwd_delta_kernel<128, false><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
-                                                                          b.Sq, p.Sq_pad);
-    } else {
-        if (b.f16)
-            bwd_delta_kernel<64, true><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
-                                                                        b.Sq, p.Sq_pad);
-        else
-            bwd_delta_kernel<64, false><<<(int)blocks, 256, 0, stream>>>(dO, O, b.lse, b.ws_lse2, b.ws_delta, n_rows,
-                                                                         b.Sq, p.Sq_pad);
-    }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], stream)) != cudaSuccess) return e;
 
     const int items_a = p.n_kt * b.B * b.Hkv, items_b = p.n_qt * b.B * b.Hq;
@@ -984,10 +1014,10 @@ cudaError_t launch_backward_bf16(const BwdProblem& b, const CUtensorMap& tq, con
     const int grid_b = items_b < b.num_sms ? items_b : b.num_sms;
     const bool cap = b.softcap > 0.f, ali = b.slopes != nullptr;
     if (b.D == 128)
-        return b.f16 ? launch_flags<128, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev)
-                     : launch_flags<128, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev);
-    return b.f16 ? launch_flags<64, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev)
-                 : launch_flags<64, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, stream, ev);
+        return b.f16 ? launch_flags<128, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, to, stream, ev)
+                     : launch_flags<128, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, to, stream, ev);
+    return b.f16 ? launch_flags<64, true>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, to, stream, ev)
+                 : launch_flags<64, false>(p, grid_a, grid_b, cap, ali, tq, tdo, tk, tv, to, stream, ev);
 }
 
 }  // namespace gbattn

@@ -128,11 +128,12 @@ cudaError_t launch_prefill_f32(const FwdProblem& p, cudaStream_t stream);
 cudaError_t launch_decode_bf16(const DecodeProblem& p, const CUtensorMap& tk, const CUtensorMap& tv,
                                cudaStream_t stream);
 
-// ev (optional, 4 events) is recorded before the prep launches, before the
-// dK / dV launch, before the dQ launch and after it.
+// to maps the forward output O (read for Delta).  ev (optional, 4 events) is
+// recorded before the prep launch, before the dQ launch, before the dK / dV
+// launch and after it.
 cudaError_t launch_backward_bf16(const BwdProblem& p, const CUtensorMap& tq, const CUtensorMap& tdo,
-                                 const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t stream,
-                                 cudaEvent_t* ev = nullptr);
+                                 const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                                 cudaStream_t stream, cudaEvent_t* ev = nullptr);
 // The same for fp32 inputs (SIMT).
 cudaError_t launch_backward_f32(const BwdProblem& p, cudaStream_t stream, cudaEvent_t* ev = nullptr);
 // The backward's first launch (both storage types): each query row's admissible
