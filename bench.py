@@ -187,14 +187,14 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # (kernel, workload, source fingerprint): bytes per launch, one-pass ncu
     # captures of the full-size workloads (values as ncu prints them)
-    ("prefill", "bf16_causal_b4_h32_s2048_d128", "63ac4a96265bae59"): 130319360,
-    ("prefill", "bf16_causal_b1_h32_s8192_d128", "63ac4a96265bae59"): 133592064,
-    ("prefill", "bf16_masked_b2_h16_s4096_d64", "63ac4a96265bae59"): 51061504,
-    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "63ac4a96265bae59"): 1789548544,
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "809a4f93da2a3b07"): 2154978304,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "809a4f93da2a3b07"): 1747040512,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "418e97a5dca29fde"): 338917376,
-    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "418e97a5dca29fde"): 216192256,
+    ("prefill", "bf16_causal_b4_h32_s2048_d128", "9c79f61dcc9de1e5"): 130435328,
+    ("prefill", "bf16_causal_b1_h32_s8192_d128", "9c79f61dcc9de1e5"): 134017280,
+    ("prefill", "bf16_masked_b2_h16_s4096_d64", "9c79f61dcc9de1e5"): 51230464,
+    ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "9c79f61dcc9de1e5"): 1779241984,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "fd02b7be27b0da85"): 2154950912,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "fd02b7be27b0da85"): 1746819840,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "042fcd65f6122d1e"): 337790976,
+    ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "042fcd65f6122d1e"): 296857600,
 }
 
 
@@ -657,7 +657,7 @@ def bench_backward(g, args, ws, dev, pk):
             "value": round(tf * ws, 2), "unit": "TFLOP/s", "ms_per_step": round(per, 4), "flops_per_step": flops,
             "flops_convention": "5 products x 2 D per admissible pair; the pages' cost line counts 12 D "
                                 "(a 4 D forward recompute)",
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 3 * args.steps,  # row intervals, dQ (with Delta), dK / dV
             "cpu_baseline": cpu,
             "phase_ms": {"prep": round(prep_ms, 4), "dkdv": round(dkdv_ms, 4), "dq": round(dq_ms, 4)},
             "roofline": {"bound": "tensor", "kernel": "bwd_kernel dK/dV (S, dP, dV, dK: 8 D flops per pair)",
