@@ -195,3 +195,24 @@ def test_bwd_fp32_row_bounds_given_forward(cuda_device):
     grads, _ = _run(cuda_device, B, 2, 2, S, S, 64, seed=14, dtype=F32, rowb=rowb, alibi=True, given_fwd=True)
     empty = rowb[..., 0] > rowb[..., 1]
     assert empty.any() and (grads[0].cpu().permute(0, 2, 1, 3)[empty] == 0).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_bwd_phase_times_form(cuda_device, dtype):
+    """attn_bwd_phase_times writes the same gradients as attn_bwd and four phase
+    times in the order (forward recompute, prep, dK / dV, dQ), whatever order
+    the launches run in (the 16-bit path runs dQ first)."""
+    import tiled_scaled_dot_gb300 as g
+    B, Hq, Hkv, S, D = 2, 8, 2, 512, 128
+    q, k, v, do = (t.to(cuda_device) for t in _inputs(B, Hq, Hkv, S, S, D, 9, dtype))
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=cuda_device)
+    out = g.attn_fwd(q, k, v, causal=True, lse=lse)
+    ref = g.attn_bwd(q, k, v, do, out, lse, causal=True)
+    *grads, phases = g.attn_bwd(q, k, v, do, out, lse, causal=True, phase_times_reps=3)
+    torch.cuda.synchronize()
+    assert g.device_status() == 0
+    for x, y in zip(ref, grads):
+        assert torch.equal(x, y)
+    assert len(phases) == 4 and all(t >= 0.0 for t in phases)
+    fwd, prep, dkdv, dq = phases
+    assert fwd < 0.05 and dkdv > 0.0 and dq > 0.0  # out and lse given: no recompute
