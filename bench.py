@@ -191,8 +191,8 @@ NCU_TRAFFIC = {
     ("prefill", "bf16_causal_b1_h32_s8192_d128", "9c79f61dcc9de1e5"): 134017280,
     ("prefill", "bf16_masked_b2_h16_s4096_d64", "9c79f61dcc9de1e5"): 51230464,
     ("prefill", "bf16_varlen_causal_b32_h32_kv8_len512-4096_d128", "9c79f61dcc9de1e5"): 1779241984,
-    ("decode", "bf16_decode_b64_h32_sk8192_d128", "fd02b7be27b0da85"): 2154950912,
-    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "fd02b7be27b0da85"): 1746819840,
+    ("decode", "bf16_decode_b64_h32_sk8192_d128", "2661c8e8b5421807"): 2154888448,
+    ("decode", "bf16_paged_decode_b64_h32_kv8_ctx4096-8192_bs64_d128", "2661c8e8b5421807"): 1746260224,
     ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dkdv", "042fcd65f6122d1e"): 337790976,
     ("backward", "bf16_causal_bwd_b4_h32_kv8_s2048_d128:dq", "042fcd65f6122d1e"): 296857600,
 }

@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         }
     }
     __syncthreads();
+    // the combine (a programmatic dependent launch) may be scheduled once every
+    // CTA of this grid has started; it waits on the device for this grid's end
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     WaitCtl wc{&abort_flag, p.status, p.timeout_ns};
 
     // Every role walks the same runs.  Contiguous: each thread keeps its own

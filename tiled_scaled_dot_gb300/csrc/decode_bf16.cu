@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
         fence_mbar_init();
     }
     __syncthreads();
+    // the combine (a programmatic dependent launch) may be scheduled once every
+    // CTA of this grid has started; it waits on the device for this grid's end
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     WaitCtl wc{&abort_flag, p.status, p.timeout_ns};
 
     if (warp == CONSUMERS) {
@@ -475,25 +478,30 @@ cudaError_t launch_decode_bf16(const DecodeProblem& f, const CUtensorMap& tk, co
                       : launch_dec_flags<64, 1>(p, cap, ali, paged, f16, tk, tv, stream);
     }
     if (e != cudaSuccess || p.num_splits == 1) return e;
-    // every partial lse is in base 2 (logits carry the log2(e) factor)
+    // every partial lse is in base 2 (logits carry the log2(e) factor).  The
+    // combine is a programmatic dependent launch: its blocks are scheduled
+    // while the decode kernel drains and wait for its completion on the device.
     const uint32_t* lens = paged ? p.context_lens : nullptr;
-    const unsigned rows = (unsigned)(p.B * p.Hq);
-    if (f.D == 128) {
-        if (f16)
-            decode_combine_kernel<128, true><<<rows, 128, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
-                                                                       LN2, lens, p.Hq);
-        else
-            decode_combine_kernel<128, false><<<rows, 128, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
-                                                                        LN2, lens, p.Hq);
-    } else {
-        if (f16)
-            decode_combine_kernel<64, true><<<rows, 64, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
-                                                                     LN2, lens, p.Hq);
-        else
-            decode_combine_kernel<64, false><<<rows, 64, 0, stream>>>(p.ws_o, p.ws_lse, p.out, p.lse, p.num_splits,
-                                                                      LN2, lens, p.Hq);
-    }
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.B * p.Hq));
+    cfg.blockDim = dim3((unsigned)f.D);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float* wo = p.ws_o;
+    const float* wl = p.ws_lse;
+    if (f.D == 128)
+        return f16 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<128, true>, wo, wl, p.out, p.lse, p.num_splits, LN2,
+                                        lens, p.Hq)
+                   : cudaLaunchKernelEx(&cfg, decode_combine_kernel<128, false>, wo, wl, p.out, p.lse, p.num_splits,
+                                        LN2, lens, p.Hq);
+    return f16 ? cudaLaunchKernelEx(&cfg, decode_combine_kernel<64, true>, wo, wl, p.out, p.lse, p.num_splits, LN2, lens,
+                                    p.Hq)
+               : cudaLaunchKernelEx(&cfg, decode_combine_kernel<64, false>, wo, wl, p.out, p.lse, p.num_splits, LN2, lens,
+                                    p.Hq);
 }
 
 }  // namespace gbattn

@@ -215,8 +215,11 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const float* __restri
                                                            const uint32_t* __restrict__ context_lens, int Hq) {
     const size_t row = blockIdx.x;
     const int d = threadIdx.x;
-    const float* ls = ws_lse + row * num_splits;
     const bool empty = context_lens && __ldg(context_lens + row / Hq) == 0u;
+    // launched as a programmatic dependent of the decode kernel: its partials
+    // are complete and visible after this wait
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float* ls = ws_lse + row * num_splits;
     float M = -INFINITY;
     if (!empty)
         for (int s = 0; s < num_splits; ++s) M = fmaxf(M, ls[s]);
