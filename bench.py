@@ -21,7 +21,10 @@ A step is one pass of the hot path over one batch of synthetic input:
     empty rows, timed like the headline.
 value = causal-adjusted attention TFLOP/s (4 D flops per admissible
 (query, key) pair) over all ranks.  The decode object reports HBM GB/s of its
-algorithmic bytes (Q + K + V + O).
+algorithmic bytes (Q + K + V + O).  e2e = the headline through attn_fwd with
+Q, K, V in pinned host memory and O copied back every step (steps pipelined
+over two streams); e2e.link = pinned copies of one step's bytes, up and down
+at once with no kernel, timed in the same run: the host link's own floor.
 
 --impl reference runs the float64 CPU oracle (the only other implementation
 of the method here) on a bounded row sample of the same workload.
